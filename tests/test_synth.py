@@ -1,0 +1,73 @@
+"""The seeded input generator: SplitMix64 evaluated with torch int64 ops must equal
+the scalar definition, and the drawn blocks must have the stated distributions."""
+import numpy as np
+import torch
+
+from gguf_q4_dequant_gb300 import synth
+
+
+def test_stream_matches_scalar_definition():
+    for seed in (0, 1, 0x51344B00, (1 << 63) + 12345, (1 << 64) - 1):
+        vals = synth.stream(seed, 1000, 300).tolist()
+        ref = [synth.splitmix64_py(seed, i) for i in range(1000, 1300)]
+        assert [v & synth.MASK64 for v in vals] == ref
+
+
+def test_block_fields_and_ranges():
+    blk = synth.blocks(synth.weight_seed(0, 0, "q_proj"), 0, 4096)
+    assert blk.shape == (4096, 144) and blk.dtype == torch.uint8
+    d = blk[:, 0:2].contiguous().view(torch.float16).float()
+    dmin = blk[:, 2:4].contiguous().view(torch.float16).float()
+    for v in (d, dmin):
+        assert torch.all(v >= 0.00099945) and torch.all(v <= 0.02001953)
+        assert float(v.mean()) == pytest_approx(0.0105, 0.001)
+    sc = blk[:, 4:16].float()
+    qs = blk[:, 16:].float()
+    assert abs(float(sc.mean()) - 127.5) < 2.0
+    assert abs(float((blk[:, 16:] & 15).float().mean()) - 7.5) < 0.1
+    assert abs(float((blk[:, 16:] >> 4).float().mean()) - 7.5) < 0.1
+    assert qs.min() == 0 and qs.max() == 255
+
+
+def pytest_approx(center, tol):
+    class _A:
+        def __eq__(self, other):
+            return abs(other - center) <= tol
+    return _A()
+
+
+def test_block_bytes_are_the_stream_bytes():
+    seed, g = 12345, 77
+    blk = synth.blocks(seed, g, 1)[0].numpy()
+    vals = [synth.splitmix64_py(seed, 19 * g + t) for t in range(19)]
+    raw = b"".join(v.to_bytes(8, "little") for v in vals[1:])
+    assert bytes(blk[4:12]) == raw[0:8]
+    assert bytes(blk[12:16]) == raw[8:12]
+    assert bytes(blk[16:144]) == raw[16:144]
+    u_d = (vals[0] >> 40) / 2.0 ** 24
+    d = np.float16(np.float32(np.float32(u_d) * np.float32(0.019)) + np.float32(0.001))
+    assert int(blk[0]) | (int(blk[1]) << 8) == int(d.view(np.uint16))
+
+
+def test_weight_rows_slices_agree():
+    seed, N, K = 99, 37, 768
+    full = synth.weight_rows(seed, N, K, chunk_blocks=7)
+    part = synth.weight_rows(seed, N, K, row0=11, nrows=9)
+    assert torch.equal(full[11:20], part)
+    samp = synth.weight_sample_rows(seed, N, K, [36, 0, 5])
+    assert torch.equal(samp, full[[36, 0, 5]])
+
+
+def test_activations():
+    x = synth.activations(5, 64, 1024)
+    assert x.dtype == torch.float32 and x.shape == (64, 1024)
+    assert abs(float(x.mean())) < 0.02 and abs(float(x.std()) - 1.0) < 0.02
+    xb = synth.activations(5, 64, 1024, torch.bfloat16)
+    assert torch.equal(xb, x.to(torch.bfloat16))
+    assert torch.equal(synth.activations(5, 64, 1024), x)
+
+
+def test_workload_sizes():
+    sizes = {i: w.packed_bytes() for i, w in synth.WORKLOADS.items()}
+    assert sizes == {0: 73728, 1: 547356672, 2: 1807073280, 3: 3906994176, 4: 7431782400}
+    assert [len(w.matrices()) for w in synth.WORKLOADS.values()] == [1, 112, 197, 252, 280]
