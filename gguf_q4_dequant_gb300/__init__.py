@@ -1,0 +1,153 @@
+"""Python binding of libq4k, the GB300 packed Q4_K dequant-matmul library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/q4k.h``. The functions mirror
+the C names and take torch tensors (device memory, caller-owned) or raw device
+pointers (ints). There is no fallback: if ``libq4k.so`` has not been built, or
+a call fails, a ``Q4KError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libq4k.so")
+
+Q4K_OK = 0
+Q4K_ERR_NULL = -1
+Q4K_ERR_BAD_DIM = -2
+Q4K_ERR_CUDA = -3
+Q4K_ERR_ALIGN = -4
+Q4K_ERR_ARCH = -5
+Q4K_ERR_TIMEOUT = -6
+
+#: every symbol include/q4k.h declares
+EXPORTS = ("q4k_status_string", "q4k_init", "q4k_dequant", "q4k_matmul", "q4k_matmul_bf16",
+           "q4k_device_error")
+
+
+_STATUS_NAMES = {Q4K_OK: "Q4K_OK", Q4K_ERR_NULL: "Q4K_ERR_NULL", Q4K_ERR_BAD_DIM: "Q4K_ERR_BAD_DIM",
+                 Q4K_ERR_CUDA: "Q4K_ERR_CUDA", Q4K_ERR_ALIGN: "Q4K_ERR_ALIGN",
+                 Q4K_ERR_ARCH: "Q4K_ERR_ARCH", Q4K_ERR_TIMEOUT: "Q4K_ERR_TIMEOUT"}
+
+
+class Q4KError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS_NAMES.get(status, 'unknown status')} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libq4k.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise Q4KError(Q4K_ERR_CUDA, f"libq4k.so not built at {LIB_PATH} "
+                               "(run gguf_q4_dequant_gb300.build.build())")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64 = ctypes.c_void_p, ctypes.c_int64
+            L.q4k_status_string.argtypes = [ctypes.c_int]
+            L.q4k_status_string.restype = ctypes.c_char_p
+            L.q4k_init.argtypes = []
+            L.q4k_init.restype = ctypes.c_int
+            L.q4k_dequant.argtypes = [vp, i64, i64, vp, vp]
+            L.q4k_dequant.restype = ctypes.c_int
+            L.q4k_matmul.argtypes = [vp, i64, i64, vp, i64, vp, vp]
+            L.q4k_matmul.restype = ctypes.c_int
+            L.q4k_matmul_bf16.argtypes = [vp, i64, i64, vp, i64, vp, vp]
+            L.q4k_matmul_bf16.restype = ctypes.c_int
+            L.q4k_device_error.argtypes = [ctypes.c_int]
+            L.q4k_device_error.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().q4k_status_string(int(status)).decode()
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("tensor must live in CUDA device memory")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != Q4K_OK:
+        raise Q4KError(rc, where)
+
+
+def _check_dtype(t, dtype, name):
+    if not isinstance(t, int) and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def q4k_init():
+    _check(lib().q4k_init(), "q4k_init")
+
+
+def q4k_dequant(W, N: int, K: int, out, stream=None):
+    """out[n*K + k] = w(n, k): packed uint8 W -> fp32 out (both on the device)."""
+    import torch
+    _check_dtype(W, torch.uint8, "W")
+    _check_dtype(out, torch.float32, "out")
+    _check(lib().q4k_dequant(_ptr(W), N, K, _ptr(out), _stream(stream)), "q4k_dequant")
+
+
+def q4k_matmul(W, N: int, K: int, X, M: int, Y, stream=None):
+    """Y[M, N] = X[M, K] (fp32) * W^T."""
+    import torch
+    _check_dtype(W, torch.uint8, "W")
+    _check_dtype(X, torch.float32, "X")
+    _check_dtype(Y, torch.float32, "Y")
+    _check(lib().q4k_matmul(_ptr(W), N, K, _ptr(X), M, _ptr(Y), _stream(stream)), "q4k_matmul")
+
+
+def q4k_matmul_bf16(W, N: int, K: int, X, M: int, Y, stream=None):
+    """Y[M, N] = X[M, K] (bf16) * W^T."""
+    import torch
+    _check_dtype(W, torch.uint8, "W")
+    _check_dtype(X, torch.bfloat16, "X")
+    _check_dtype(Y, torch.float32, "Y")
+    _check(lib().q4k_matmul_bf16(_ptr(W), N, K, _ptr(X), M, _ptr(Y), _stream(stream)),
+           "q4k_matmul_bf16")
+
+
+def q4k_device_error(clear: bool = True) -> int:
+    """Status of the device error word (synchronous)."""
+    return lib().q4k_device_error(1 if clear else 0)
+
+
+def matmul(W, N: int, K: int, X, Y=None, stream=None):
+    """Convenience: dispatch on X's dtype, allocating Y with torch if not given."""
+    import torch
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    if X.dtype == torch.bfloat16:
+        q4k_matmul_bf16(W, N, K, X, M, Y, stream)
+    else:
+        q4k_matmul(W, N, K, X, M, Y, stream)
+    return Y

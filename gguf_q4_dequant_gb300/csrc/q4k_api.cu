@@ -1,0 +1,223 @@
+// q4k_api.cu -- the C ABI of libq4k (include/q4k.h): argument checks, one-time
+// per-device set-up, TMA descriptor encoding and dispatch by M.
+//
+// Dispatch (the decode / prefill split of the rlx-llama32 page's "Decode" and
+// "Packed GGUF" sections):
+//   q4k_dequant              -> K1 dequant_kernel
+//   q4k_matmul      M <= 16  -> K2 gemv_kernel (fp32 activations)
+//                   M >  16  -> K2 over consecutive 16-row slices of X
+//   q4k_matmul_bf16 M <= 16  -> K2 gemv_kernel (bf16 activations)
+//                   M >= 17  -> K3 gemm_kernel (tcgen05, TMEM accumulators)
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/q4k.h"
+#include "q4k_internal.h"
+
+namespace q4k {
+
+// Device error word: bit 0 = a bounded in-kernel wait ran out. Kernels receive
+// its device address (resolved per device in init_device).
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::once_flag once;
+    int status = Q4K_OK;
+    DeviceInfo info;
+};
+
+DeviceState g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+void init_device(int dev, DeviceState& st) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+        st.status = Q4K_ERR_CUDA;
+        return;
+    }
+    if (prop.major != 10 || prop.minor != 3) {
+        st.status = Q4K_ERR_ARCH;
+        return;
+    }
+    st.info.num_sms = prop.multiProcessorCount;
+    st.info.max_smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || gemv_setup() != cudaSuccess ||
+        gemm_setup() != cudaSuccess || encoder() == nullptr) {
+        st.status = Q4K_ERR_CUDA;
+        return;
+    }
+    st.info.err = static_cast<unsigned int*>(p);
+    st.status = Q4K_OK;
+}
+
+int current_device(const DeviceInfo** info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return Q4K_ERR_CUDA;
+    DeviceState& st = g_dev[dev];
+    std::call_once(st.once, [&] { init_device(dev, st); });
+    if (st.status != Q4K_OK) return st.status;
+    *info = &st.info;
+    return Q4K_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Limits keep every index the kernels form in 32 bits where they use int.
+int check_dims(int64_t N, int64_t K) {
+    if (N < 1 || K < 256 || K % 256 != 0) return Q4K_ERR_BAD_DIM;
+    if (N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 24)) return Q4K_ERR_BAD_DIM;
+    return Q4K_OK;
+}
+
+// W as a 2-D byte tensor {K/256*144, N}; box = one super-block of `rows` rows.
+int encode_w(CUtensorMap* map, const void* W, int64_t N, int64_t K, int rows) {
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 256) * 144;
+    const cuuint64_t dims[2] = {row_bytes, static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {144, static_cast<cuuint32_t>(rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encoder()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+// X as a 2-D bf16 tensor {K, M}; box {64, BN} with the 128-byte swizzle.
+int encode_x_bf16(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BN)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+int run_gemv(const void* W, int64_t N, int64_t K, const void* X, bool xb, int64_t M, float* Y,
+             cudaStream_t stream, const DeviceInfo& dev) {
+    CUtensorMap tw;
+    int rc = encode_w(&tw, W, N, K, 32);
+    if (rc != Q4K_OK) return rc;
+    const size_t xelem = xb ? 2 : 4;
+    for (int64_t m0 = 0; m0 < M; m0 += 16) {
+        const int mc = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
+        const void* Xc = static_cast<const uint8_t*>(X) + static_cast<size_t>(m0) * K * xelem;
+        if (launch_gemv(tw, Xc, xb, mc, static_cast<int>(N), static_cast<int>(K), Y + m0 * N, stream,
+                        dev) != cudaSuccess)
+            return Q4K_ERR_CUDA;
+    }
+    return Q4K_OK;
+}
+
+}  // namespace
+}  // namespace q4k
+
+using namespace q4k;
+
+extern "C" {
+
+const char* q4k_status_string(int status) {
+    switch (status) {
+        case Q4K_OK: return "Q4K_OK";
+        case Q4K_ERR_NULL: return "Q4K_ERR_NULL: a required pointer is NULL";
+        case Q4K_ERR_BAD_DIM: return "Q4K_ERR_BAD_DIM: need N >= 1, M >= 1, K >= 256, K % 256 == 0";
+        case Q4K_ERR_CUDA: return "Q4K_ERR_CUDA: a CUDA call or kernel launch failed";
+        case Q4K_ERR_ALIGN: return "Q4K_ERR_ALIGN: W, X, Y and out must be 16-byte aligned";
+        case Q4K_ERR_ARCH: return "Q4K_ERR_ARCH: the current device is not compute capability 10.3";
+        case Q4K_ERR_TIMEOUT: return "Q4K_ERR_TIMEOUT: an in-kernel wait ran out of time";
+    }
+    return "unknown q4k status";
+}
+
+int q4k_init(void) {
+    const DeviceInfo* info = nullptr;
+    return current_device(&info);
+}
+
+int q4k_dequant(const void* W, int64_t N, int64_t K, float* out_f32, void* stream) {
+    if (!W || !out_f32) return Q4K_ERR_NULL;
+    int rc = check_dims(N, K);
+    if (rc != Q4K_OK) return rc;
+    if (!aligned16(W) || !aligned16(out_f32)) return Q4K_ERR_ALIGN;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = current_device(&dev)) != Q4K_OK) return rc;
+    if (launch_dequant(static_cast<const uint8_t*>(W), N, K, out_f32,
+                       static_cast<cudaStream_t>(stream), dev->num_sms) != cudaSuccess)
+        return Q4K_ERR_CUDA;
+    return Q4K_OK;
+}
+
+int q4k_matmul(const void* W, int64_t N, int64_t K, const float* X, int64_t M, float* Y,
+               void* stream) {
+    if (!W || !X || !Y) return Q4K_ERR_NULL;
+    int rc = check_dims(N, K);
+    if (rc != Q4K_OK) return rc;
+    if (M < 1 || M > (int64_t(1) << 31) - 1) return Q4K_ERR_BAD_DIM;
+    if (!aligned16(W) || !aligned16(X) || !aligned16(Y)) return Q4K_ERR_ALIGN;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = current_device(&dev)) != Q4K_OK) return rc;
+    return run_gemv(W, N, K, X, false, M, Y, static_cast<cudaStream_t>(stream), *dev);
+}
+
+int q4k_matmul_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16, int64_t M,
+                    float* Y, void* stream) {
+    if (!W || !X_bf16 || !Y) return Q4K_ERR_NULL;
+    int rc = check_dims(N, K);
+    if (rc != Q4K_OK) return rc;
+    if (M < 1 || M > (int64_t(1) << 31) - 1) return Q4K_ERR_BAD_DIM;
+    if (!aligned16(W) || !aligned16(X_bf16) || !aligned16(Y)) return Q4K_ERR_ALIGN;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = current_device(&dev)) != Q4K_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M <= 16) return run_gemv(W, N, K, X_bf16, true, M, Y, st, *dev);
+    const int BN = gemm_pick_bn(static_cast<int>(M));
+    CUtensorMap tw, tx;
+    if ((rc = encode_w(&tw, W, N, K, 128)) != Q4K_OK) return rc;
+    if ((rc = encode_x_bf16(&tx, X_bf16, M, K, BN)) != Q4K_OK) return rc;
+    if (launch_gemm(tw, tx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), Y, BN, st,
+                    *dev) != cudaSuccess)
+        return Q4K_ERR_CUDA;
+    return Q4K_OK;
+}
+
+int q4k_device_error(int clear) {
+    const DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != Q4K_OK) return rc;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return Q4K_ERR_CUDA;
+    if (clear && v) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return Q4K_ERR_CUDA;
+    }
+    return v ? Q4K_ERR_TIMEOUT : Q4K_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,34 @@
+// q4k_internal.h -- host-side launchers shared between the C ABI shim and the
+// kernel translation units. Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q4k {
+
+struct DeviceInfo {
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    unsigned int* err = nullptr;  // device address of the device error word
+};
+
+cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, cudaStream_t stream,
+                           int num_sms);
+
+// Split-K GEMV for 1 <= M <= 16 rows of activations (fp32 or bf16 bit patterns).
+// tmapW: 2-D uint8 map {K/256*144, N}, box {144, 32}.
+cudaError_t launch_gemv(const CUtensorMap& tmapW, const void* X, bool x_bf16, int M, int N, int K,
+                        float* Y, cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t gemv_setup();
+
+// tcgen05 GEMM for M >= 17 rows of bf16 activations.
+// tmapW: 2-D uint8 map {K/256*144, N}, box {144, 128}; tmapX: 2-D bf16 map
+// {K, M}, box {64, BN}, 128-byte swizzle.
+int gemm_pick_bn(int M);
+cudaError_t launch_gemm(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
+                        float* Y, int BN, cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t gemm_setup();
+
+}  // namespace q4k

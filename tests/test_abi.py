@@ -1,0 +1,89 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every
+symbol include/q4k.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gguf_q4_dequant_gb300 as q4k_pkg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "q4k.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4k_\w+)\s*\(", text)))
+
+
+def test_header_matches_binding_exports():
+    assert _declared_functions() == sorted(q4k_pkg.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(q4k):
+    L = ctypes.CDLL(q4k.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(q4k):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = q4k.status_string(code)
+        assert s.startswith("Q4K_")
+    assert q4k.status_string(7) == "unknown q4k status"
+
+
+# Host-side checks happen before the library touches the device, so they run
+# here without a GPU. Pointers are plain integers that are never dereferenced.
+A16 = 1 << 20  # a 16-byte-aligned fake address
+
+
+@pytest.mark.parametrize("call", ["dequant", "matmul", "matmul_bf16"])
+def test_null_pointers_rejected(q4k, call):
+    L = q4k.lib()
+    if call == "dequant":
+        assert L.q4k_dequant(None, 4, 256, A16, None) == q4k.Q4K_ERR_NULL
+        assert L.q4k_dequant(A16, 4, 256, None, None) == q4k.Q4K_ERR_NULL
+    else:
+        f = L.q4k_matmul if call == "matmul" else L.q4k_matmul_bf16
+        assert f(None, 4, 256, A16, 1, A16, None) == q4k.Q4K_ERR_NULL
+        assert f(A16, 4, 256, None, 1, A16, None) == q4k.Q4K_ERR_NULL
+        assert f(A16, 4, 256, A16, 1, None, None) == q4k.Q4K_ERR_NULL
+
+
+@pytest.mark.parametrize("N,K,M", [(0, 256, 1), (-3, 256, 1), (4, 0, 1), (4, 255, 1), (4, 384, 1),
+                                   (4, 128, 1), (4, 256, 0), (4, 256, -1), (1 << 31, 256, 1),
+                                   (4, (1 << 24) + 256, 1)])
+def test_bad_dims_rejected(q4k, N, K, M):
+    L = q4k.lib()
+    assert L.q4k_matmul(A16, N, K, A16, M, A16, None) == q4k.Q4K_ERR_BAD_DIM
+    assert L.q4k_matmul_bf16(A16, N, K, A16, M, A16, None) == q4k.Q4K_ERR_BAD_DIM
+    if M >= 1:
+        assert L.q4k_dequant(A16, N, K, A16, None) == q4k.Q4K_ERR_BAD_DIM
+
+
+def test_misaligned_pointers_rejected(q4k):
+    L = q4k.lib()
+    for off in (1, 4, 8):
+        assert L.q4k_dequant(A16 + off, 4, 256, A16, None) == q4k.Q4K_ERR_ALIGN
+        assert L.q4k_dequant(A16, 4, 256, A16 + off, None) == q4k.Q4K_ERR_ALIGN
+        assert L.q4k_matmul(A16, 4, 256, A16 + off, 1, A16, None) == q4k.Q4K_ERR_ALIGN
+        assert L.q4k_matmul_bf16(A16, 4, 256, A16, 1, A16 + off, None) == q4k.Q4K_ERR_ALIGN
+
+
+def test_binding_rejects_wrong_dtypes(q4k):
+    torch = pytest.importorskip("torch")
+    W = torch.zeros(144, dtype=torch.int8)
+    with pytest.raises(ValueError):
+        q4k.q4k_matmul(W, 1, 256, 0, 1, 0, stream=0)
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    import gguf_q4_dequant_gb300 as m
+    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m, "LIB_PATH", "/nonexistent/libq4k.so")
+    with pytest.raises(m.Q4KError):
+        m.lib()

@@ -1,0 +1,272 @@
+"""GPU parity: libq4k (through its C ABI) against the CPU oracle, element by element.
+
+Bars: dequant bit-exact; GEMV (M <= 16, fp32 or bf16 activations) within
+1e-4 * sum_k |x*w| per output; tcgen05 GEMM (bf16 activations, M >= 17) within
+5e-3 * sum_k |x*w| per output. Inputs are drawn on the host by the seeded
+generator and copied to the device; expected values come from the oracle only.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gguf_q4_dequant_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_GEMV = 1e-4
+TOL_GEMM = 5e-3
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda(q4k):
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    torch.cuda.set_device(0)
+    q4k.q4k_init()
+    yield
+    torch.cuda.synchronize()
+    assert q4k.q4k_device_error() == 0
+
+
+def _x_for_oracle(oracle_mod, X):
+    if X.dtype == torch.bfloat16:
+        return oracle_mod.bf16_to_f32(X.view(torch.int16).numpy().view(np.uint16))
+    return X.numpy()
+
+
+def _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X, tol, rows=None, W_rows=None):
+    """Runs the library on (Wd, X) and compares the columns `rows` (all if None)."""
+    M = X.shape[0]
+    Y = torch.full((M, N), float("nan"), device=DEV)
+    q4k.matmul(Wd, N, K, X.to(DEV), Y)
+    torch.cuda.synchronize()
+    Xo = _x_for_oracle(oracle_mod, X)
+    if rows is None:
+        Yref, A = oracle_mod.matmul(Wh.numpy(), N, K, Xo)
+        got = Y.cpu().double().numpy()
+    else:
+        Yref, A = oracle_mod.matmul(W_rows.numpy(), len(rows), K, Xo)
+        got = Y[:, torch.as_tensor(rows, device=DEV)].cpu().double().numpy()
+    assert np.all(np.isfinite(got)), "unwritten or non-finite outputs"
+    err = np.abs(got - Yref)
+    bound = tol * A + 1e-30
+    worst = float(np.max(err / bound))
+    assert worst <= 1.0, f"max |err| / ({tol} * sum|wx|) = {worst:.3f}"
+    return worst
+
+
+# ------------------------------------------------------------------ dequant ---
+
+def _dequant_check(q4k, oracle_mod, Wh, N, K):
+    out = torch.full((N, K), float("nan"), device=DEV)
+    q4k.q4k_dequant(Wh.to(DEV), N, K, out)
+    torch.cuda.synchronize()
+    ref = oracle_mod.dequant(Wh.numpy(), N, K)
+    got = out.cpu().numpy()
+    np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (3, 512), (256, 512), (257, 1280), (64, 17408)])
+def test_dequant_bit_exact(q4k, oracle_mod, N, K):
+    _dequant_check(q4k, oracle_mod, synth.weight_rows(1000 + N, N, K), N, K)
+
+
+def test_dequant_arbitrary_fp16_scales(q4k, oracle_mod):
+    # d and dmin over (almost) all finite fp16 bit patterns, incl. subnormals and negatives
+    rng = np.random.default_rng(11)
+    N, K = 512, 1024
+    Wh = synth.weight_rows(77, N, K).numpy().reshape(-1, 144).copy()
+    bits = rng.integers(0, 1 << 16, (Wh.shape[0], 2)).astype(np.uint16)
+    bits[~np.isfinite(bits.view(np.float16))] = 0x3C00
+    Wh[:, 0:4] = bits.view(np.uint8).reshape(-1, 4)
+    _dequant_check(q4k, oracle_mod, torch.from_numpy(Wh.reshape(N, -1)), N, K)
+
+
+def test_dequant_golden_blocks(q4k, oracle_mod):
+    import test_oracle_pins as pins
+    blocks = []
+    for case in pins._golden_cases():
+        scales = [int(x, 16) for x in case["scales"].split()]
+        qs = [int(case.get("qs_fill", "00"), 16)] * 128
+        for pos, val in case.get("qs_set", {}).items():
+            qs[int(pos)] = int(val, 16)
+        blocks.append(pins.make_block(int(case["d"], 16), int(case["dmin"], 16), scales, qs))
+    Wh = torch.from_numpy(np.stack(blocks))
+    _dequant_check(q4k, oracle_mod, Wh, len(blocks), 256)
+
+
+@pytest.mark.parametrize("wl", [1, 2, 3, 4])
+def test_dequant_layer0_full_size(q4k, oracle_mod, wl):
+    w = synth.WORKLOADS[wl]
+    shapes = {(n, k): m for (_, m, n, k) in w.matrices() if _ == 0 or m == "lm_head"}
+    for (N, K), name in shapes.items():
+        Wh = synth.weight_rows(synth.weight_seed(wl, 0, name), N, K)
+        _dequant_check(q4k, oracle_mod, Wh, N, K)
+
+
+# --------------------------------------------------------------------- GEMV ---
+
+@pytest.mark.parametrize("N", [1, 7, 32, 33, 100, 300])
+@pytest.mark.parametrize("K", [256, 768, 2048])
+@pytest.mark.parametrize("xdt", ["f32", "bf16"])
+def test_gemv_ragged(q4k, oracle_mod, N, K, xdt):
+    Wh = synth.weight_rows(2000 + N + K, N, K)
+    Wd = Wh.to(DEV)
+    dt = torch.bfloat16 if xdt == "bf16" else torch.float32
+    for M in (1, 2, 3, 4, 5, 8, 9, 13, 16):
+        X = synth.activations(3000 + M + K, M, K, dt)
+        _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X, TOL_GEMV)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_gemv_tiny_workload(q4k, oracle_mod, M):
+    w = synth.WORKLOADS[0]
+    (_, name, N, K), = w.matrices()
+    Wh = synth.weight_rows(synth.weight_seed(0, 0, name), N, K)
+    X = synth.activations(synth.x_seed(0, K, M), M, K)
+    _check_matmul(q4k, oracle_mod, Wh, Wh.to(DEV), N, K, X, TOL_GEMV)
+
+
+def test_gemv_activation_scales(q4k, oracle_mod):
+    # per-block exponent handling: huge, tiny, zero and mixed-magnitude blocks
+    N, K = 96, 2048
+    Wh = synth.weight_rows(5, N, K)
+    Wd = Wh.to(DEV)
+    base = synth.activations(6, 4, K)
+    scale = torch.ones(4, K)
+    scale[0, :256] = 1e30
+    scale[0, 256:512] = 1e-30
+    scale[1, :] = 1e-38
+    scale[2, 512:768] = 0.0
+    scale[3, ::7] = 3e4
+    X = (base * scale).float()
+    _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X, TOL_GEMV)
+    _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, torch.zeros(2, K), TOL_GEMV)
+
+
+def test_fp32_large_m_runs_in_16_row_slices(q4k, oracle_mod):
+    N, K = 200, 1024
+    Wh = synth.weight_rows(9, N, K)
+    Wd = Wh.to(DEV)
+    for M in (17, 33):
+        X = synth.activations(10 + M, M, K)
+        _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X, TOL_GEMV)
+        Y = q4k.matmul(Wd, N, K, X.to(DEV))
+        Y16 = torch.cat([q4k.matmul(Wd, N, K, X[i:i + 16].contiguous().to(DEV))
+                         for i in range(0, M, 16)])
+        assert torch.equal(Y, Y16)
+
+
+# --------------------------------------------------------------------- GEMM ---
+
+@pytest.mark.parametrize("M", [17, 31, 32, 33, 64, 65, 100, 128, 129, 255, 256, 257, 512])
+def test_gemm_ragged(q4k, oracle_mod, M):
+    for (N, K) in ((128, 256), (200, 1024), (384, 512)):
+        Wh = synth.weight_rows(4000 + N + K, N, K)
+        X = synth.activations(5000 + M + K, M, K, torch.bfloat16)
+        _check_matmul(q4k, oracle_mod, Wh, Wh.to(DEV), N, K, X, TOL_GEMM)
+
+
+def test_gemm_long_k(q4k, oracle_mod):
+    N, K, M = 256, 12288, 300
+    Wh = synth.weight_rows(6000, N, K)
+    X = synth.activations(6001, M, K, torch.bfloat16)
+    _check_matmul(q4k, oracle_mod, Wh, Wh.to(DEV), N, K, X, TOL_GEMM)
+
+
+def test_dispatch_boundary_16_17(q4k, oracle_mod):
+    N, K = 160, 512
+    Wh = synth.weight_rows(7000, N, K)
+    Wd = Wh.to(DEV)
+    for M, tol in ((16, TOL_GEMV), (17, TOL_GEMM)):
+        X = synth.activations(7001 + M, M, K, torch.bfloat16)
+        _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X, tol)
+
+
+# ------------------------------------------------------------- full sizes ---
+
+def _sample_rows(N, n=256, seed=0):
+    rng = np.random.default_rng(seed + N)
+    pick = set(rng.choice(N, size=min(N, n), replace=False).tolist())
+    pick |= {0, 1, N - 2, N - 1}
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("wl", [1, 2, 3, 4])
+def test_full_size_sampled(q4k, oracle_mod, wl):
+    """Layer-0 matrices (and the lm_head) at full size, in the launch
+    configuration the benchmark times; sampled output columns are compared with
+    the oracle, and the device-drawn weights are checked against the host draw."""
+    w = synth.WORKLOADS[wl]
+    mats = [(m, n, k) for (layer, m, n, k) in w.matrices() if layer == 0 or m == "lm_head"]
+    cases = [(M, "f32") for M in w.decode_m if "f32" in w.x_dtypes]
+    cases += [(M, "bf16") for M in w.decode_m if "bf16" in w.x_dtypes]
+    cases += [(M, "bf16") for M in w.prefill_m]
+    for name, N, K in mats:
+        seed = synth.weight_seed(wl, 0, name)
+        Wd = synth.weight_rows(seed, N, K, device=DEV)
+        rows = _sample_rows(N)
+        W_rows = synth.weight_sample_rows(seed, N, K, rows)
+        assert torch.equal(Wd[torch.as_tensor(rows, device=DEV)].cpu(), W_rows)
+        for M, xdt in cases:
+            dt = torch.bfloat16 if xdt == "bf16" else torch.float32
+            X = synth.activations(synth.x_seed(wl, K, M), M, K, dt)
+            tol = TOL_GEMM if (dt == torch.bfloat16 and M > 16) else TOL_GEMV
+            _check_matmul(q4k, oracle_mod, None, Wd, N, K, X, tol, rows=rows, W_rows=W_rows)
+        del Wd
+        torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ plumbing ---
+
+def test_outputs_stay_inside_y(q4k):
+    N, K = 100, 512
+    Wd = synth.weight_rows(8, N, K).to(DEV)
+    for M, dt in ((3, torch.float32), (40, torch.bfloat16)):
+        X = synth.activations(9, M, K, dt).to(DEV)
+        guard = 64
+        buf = torch.full((guard + M * N + guard,), float("nan"), device=DEV)
+        Y = buf[guard:guard + M * N].view(M, N)
+        q4k.matmul(Wd, N, K, X, Y)
+        torch.cuda.synchronize()
+        assert torch.isnan(buf[:guard]).all() and torch.isnan(buf[-guard:]).all()
+        assert torch.isfinite(Y).all()
+
+
+def test_side_stream_and_graph_capture(q4k):
+    N, K = 512, 2048
+    Wd = synth.weight_rows(12, N, K).to(DEV)
+    X1 = synth.activations(13, 1, K).to(DEV)
+    Xp = synth.activations(14, 64, K, torch.bfloat16).to(DEV)
+    ref1 = q4k.matmul(Wd, N, K, X1)
+    refp = q4k.matmul(Wd, N, K, Xp)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    Y1 = torch.empty(1, N, device=DEV)
+    Yp = torch.empty(64, N, device=DEV)
+    with torch.cuda.stream(s):
+        q4k.matmul(Wd, N, K, X1, Y1)
+        q4k.matmul(Wd, N, K, Xp, Yp)
+    s.synchronize()
+    assert torch.equal(Y1, ref1) and torch.equal(Yp, refp)
+    g = torch.cuda.CUDAGraph()
+    Y1.zero_()
+    Yp.zero_()
+    with torch.cuda.graph(g):
+        q4k.matmul(Wd, N, K, X1, Y1)
+        q4k.matmul(Wd, N, K, Xp, Yp)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Y1, ref1) and torch.equal(Yp, refp)
+
+
+def test_repeat_calls_are_deterministic(q4k):
+    N, K = 300, 4096
+    Wd = synth.weight_rows(15, N, K).to(DEV)
+    for M, dt in ((1, torch.float32), (8, torch.bfloat16), (200, torch.bfloat16)):
+        X = synth.activations(16, M, K, dt).to(DEV)
+        a = q4k.matmul(Wd, N, K, X)
+        b = q4k.matmul(Wd, N, K, X)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
