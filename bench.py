@@ -43,6 +43,34 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+KERNEL_SOURCES = {
+    "gemv_kernel<1,f32>": ["gguf_q4_dequant_gb300/csrc/q4k_gemv.cu", "gguf_q4_dequant_gb300/csrc/q4k_device.cuh"],
+    "gemm_kernel<256>": ["gguf_q4_dequant_gb300/csrc/q4k_gemm.cu", "gguf_q4_dequant_gb300/csrc/q4k_device.cuh"],
+}
+
+
+def sources_sha256(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's sources changed after the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("sources_sha256") != sources_sha256(kernel):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -59,30 +87,41 @@ def _host_cores():
 
 # ------------------------------------------------------------- CPU oracle ---
 
+_HOST_DECODE = None
+
+
+def _host_decode_set():
+    """Host copies of the decode sweep's weights and activation rows (drawn once)."""
+    global _HOST_DECODE
+    if _HOST_DECODE is None:
+        from gguf_q4_dequant_gb300 import synth
+        w = synth.WORKLOADS[DECODE_WL]
+        mats = [(synth.weight_rows(synth.weight_seed(DECODE_WL, layer, name), N, K).numpy(), N, K)
+                for (layer, name, N, K) in w.matrices()]
+        xs = {K: synth.activations(synth.x_seed(DECODE_WL, K, 1), 1, K).numpy()
+              for K in {K for (_, _, K) in mats}}
+        _HOST_DECODE = (w, mats, xs)
+    return _HOST_DECODE
+
+
 def cpu_oracle_decode(budget_s: float, threads: int):
-    """Times the oracle on whole layers of the decode sweep until `budget_s`."""
-    import numpy as np
+    """Times the oracle (as it stands) over the decode sweep, matrix by matrix in
+    sweep order, until `budget_s` seconds of oracle time have elapsed."""
     import oracle
-    from gguf_q4_dequant_gb300 import synth
     oracle.build()
-    w = synth.WORKLOADS[DECODE_WL]
-    total_bytes, elapsed, layers = 0, 0.0, 0
-    xs = {}
-    for layer in range(w.layers):
-        for (name, N, K) in w.layer_shapes:
-            Wh = synth.weight_rows(synth.weight_seed(DECODE_WL, layer, name), N, K).numpy()
-            if K not in xs:
-                xs[K] = synth.activations(synth.x_seed(DECODE_WL, K, 1), 1, K).numpy()
-            t0 = time.perf_counter()
-            oracle.matmul(Wh, N, K, xs[K], threads=threads)
-            elapsed += time.perf_counter() - t0
-            total_bytes += Wh.size
-        layers += 1
-        if elapsed >= budget_s:
-            break
+    w, mats, xs = _host_decode_set()
+    total_bytes, elapsed, done = 0, 0.0, 0
+    while elapsed < budget_s:
+        Wh, N, K = mats[done % len(mats)]
+        t0 = time.perf_counter()
+        oracle.matmul(Wh, N, K, xs[K], threads=threads)
+        elapsed += time.perf_counter() - t0
+        total_bytes += Wh.size
+        done += 1
     return {"value": total_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"oracle matmul over {layers} of {w.layers} layers of the decode sweep "
-                      f"({total_bytes / 1e6:.0f} MB packed, M=1), {elapsed:.1f} s of CPU time"}
+            "sample": f"oracle matmul over {done} matrices of the decode sweep in sweep order "
+                      f"({done / len(mats):.2f} sweeps, {total_bytes / 1e6:.0f} MB packed, M=1), "
+                      f"{elapsed:.1f} s of CPU time"}
 
 
 def run_reference(args):
@@ -163,94 +202,103 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ GPU arm ---
 
-def _build_decode(dev):
-    import torch
+def _weights(wl, dev, layers):
     from gguf_q4_dequant_gb300 import synth
-    w = synth.WORKLOADS[DECODE_WL]
-    mats = []
-    for (layer, name, N, K) in w.matrices():
-        mats.append((synth.weight_rows(synth.weight_seed(DECODE_WL, layer, name), N, K, device=dev),
-                     N, K))
-    Ks = sorted({K for (_, _, K) in mats})
-    x_host = {K: synth.activations(synth.x_seed(DECODE_WL, K, 1), 1, K).pin_memory() for K in Ks}
-    x_dev = {K: x_host[K].to(dev) for K in Ks}
-    y_total = sum(N for (_, N, _) in mats)
-    y = torch.empty(y_total, device=dev)
-    return w, mats, x_host, x_dev, y
+    w = synth.WORKLOADS[wl]
+    mats = [(synth.weight_rows(synth.weight_seed(wl, layer, name), N, K, device=dev), N, K)
+            for (layer, name, N, K) in w.matrices() if not layers or layer < layers]
+    return w, mats
 
 
-def _build_prefill(dev):
-    import torch
-    from gguf_q4_dequant_gb300 import synth
-    w = synth.WORKLOADS[PREFILL_WL]
-    mats = []
-    for (layer, name, N, K) in w.matrices():
-        mats.append((synth.weight_rows(synth.weight_seed(PREFILL_WL, layer, name), N, K, device=dev),
-                     N, K))
-    Ks = sorted({K for (_, _, K) in mats})
-    x_dev = {K: synth.activations(synth.x_seed(PREFILL_WL, K, PREFILL_M), PREFILL_M, K,
-                                  torch.bfloat16).to(dev) for K in Ks}
-    y = torch.empty(PREFILL_M * max(N for (_, N, _) in mats), device=dev)
-    return w, mats, x_dev, y
-
-
-def _sweep_fn(q4k, mats, x_dev, y, M, bf16):
-    """Returns a callable issuing one sweep (one launch per matrix) on the current stream."""
+def _sweep_calls(q4k, mats, x_dev, y, M, bf16, stream_ptr):
+    """One closure per matrix, each issuing one public-API call on `stream_ptr`.
+    At M = 1 every matrix writes its own slice of `y`; at larger M they share it."""
     lib = q4k.lib()
-    calls = []
-    off = 0
-    for (Wd, N, K) in mats:
-        yp = y.data_ptr() + (off * 4 if M == 1 else 0)
-        calls.append((Wd.data_ptr(), N, K, x_dev[K].data_ptr(), yp))
-        if M == 1:
-            off += N
     fn = lib.q4k_matmul_bf16 if bf16 else lib.q4k_matmul
+    calls, off = [], 0
+    for (Wd, N, K) in mats:
+        args = (Wd.data_ptr(), N, K, x_dev[K].data_ptr(), M, y.data_ptr() + 4 * off, stream_ptr)
 
-    def run(stream_ptr):
-        for (wp, N, K, xp, yp) in calls:
-            rc = fn(wp, N, K, xp, M, yp, stream_ptr)
+        def call(a=args):
+            rc = fn(*a)
             if rc != 0:
                 raise q4k.Q4KError(rc, "sweep")
-    return run
+        calls.append(call)
+        if M == 1:
+            off += N
+    return calls
+
+
+def _capture(torch, calls, stream):
+    for c in calls:  # first use outside capture
+        c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    return g
 
 
 def _time_graph(torch, graph, stream, steps, warmup, barrier):
-    for _ in range(warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    barrier()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
-        graph.replay()
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    return start.elapsed_time(end) / steps  # ms per step
-
-
-def _per_launch_ms(torch, run_calls, stream, reps=3):
-    """Average kernel duration with CUDA events around every launch of a sweep."""
-    durs = []
-    for _ in range(reps):
-        evs = []
-        for call in run_calls:
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            call()
-            b.record(stream)
-            evs.append((a, b))
+    """ms per replay, CUDA events on the stream the graph is replayed on."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
         torch.cuda.synchronize()
-        durs.extend(a.elapsed_time(b) for a, b in evs)
-    return statistics.mean(durs)
+        barrier()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    return start.elapsed_time(end) / steps
+
+
+def run_profile_shape(args):
+    """Microbenchmark of one matrix shape: a CUDA graph of back-to-back calls over
+    enough distinct weight copies to exceed L2; prints per-launch time."""
+    import math
+    import torch
+    import gguf_q4_dequant_gb300 as q4k
+    from gguf_q4_dequant_gb300 import build as q4k_build
+    from gguf_q4_dequant_gb300 import synth
+    N, K, M = (int(v) for v in args.profile_shape.split(","))
+    q4k_build.build()
+    torch.cuda.set_device(0)
+    q4k.q4k_init()
+    q4k.q4k_set_pdl(args.pdl)
+    dev = "cuda:0"
+    wb = N * K // 256 * 144
+    R = min(64, max(2, math.ceil(args.profile_bytes / wb)))
+    Ws = [synth.weight_rows(0x5eed + i, N, K, device=dev) for i in range(R)]
+    bf16 = M > 16
+    X = synth.activations(0x5eed, M, K, torch.bfloat16 if bf16 else torch.float32).to(dev)
+    Y = torch.empty(M, N, device=dev)
+    lib = q4k.lib()
+    fn = lib.q4k_matmul_bf16 if bf16 else lib.q4k_matmul
+    stream = torch.cuda.Stream()
+    calls = [(lambda W=W: fn(W.data_ptr(), N, K, X.data_ptr(), M, Y.data_ptr(), stream.cuda_stream))
+             for W in Ws]
+    g = _capture(torch, calls, stream)
+    ms = _time_graph(torch, g, stream, args.steps, args.warmup, lambda: None)
+    us = ms * 1e3 / R
+    print(json.dumps({"shape": {"N": N, "K": K, "M": M}, "x_dtype": "bf16" if bf16 else "f32",
+                      "pdl": args.pdl, "copies": R, "us_per_launch": round(us, 3),
+                      "packed_GBps": round(wb / us / 1e3, 1),
+                      "TFLOPs": round(2 * M * N * K / us / 1e6, 2),
+                      "device_error": q4k.q4k_device_error()}))
 
 
 def run_gpu(args):
     import torch
     import gguf_q4_dequant_gb300 as q4k
     from gguf_q4_dequant_gb300 import build as q4k_build
+    from gguf_q4_dequant_gb300 import synth
     ws, rank, local = _dist()
     if ws > 1:
         import torch.distributed as dist
@@ -265,144 +313,140 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     q4k.q4k_init()
+    q4k.q4k_set_pdl(args.pdl)
     hbm, bf16_peak, bf16_sust, peak_kind = _peaks()
-
-    # ---------------------------------------------------------- decode leg ---
-    w1, mats1, x_host1, x_dev1, y1 = _build_decode(dev)
-    bytes1 = sum(Wd.numel() for (Wd, _, _) in mats1)
-    launches1 = len(mats1)
     stream = torch.cuda.Stream()
-    with torch.cuda.stream(stream):
-        sweep1 = _sweep_fn(q4k, mats1, x_dev1, y1, 1, False)
-        sweep1(stream.cuda_stream)  # first use outside capture
-        torch.cuda.synchronize()
-        g1 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g1, stream=stream):
-            sweep1(torch.cuda.current_stream().cuda_stream)
-    torch.cuda.synchronize()
-
+    sp = stream.cuda_stream
+    out = {"metric": METRIC, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded Q4_K weights, N(0,1) activations)"}
     sampler = ClockSampler(local)
     sampler.start()
-    # keep the GPU busy ~1.5 s so the clock samples reflect steady load
-    t_end = time.time() + 1.5
-    while time.time() < t_end:
-        for _ in range(50):
-            g1.replay()
-        torch.cuda.synchronize()
-    ms1 = _time_graph(torch, g1, stream, args.steps, args.warmup, barrier)
+    launches = 0
+    times = {}
 
-    # ---------------------------------------------------------- prefill leg ---
-    w3, mats3, x_dev3, y3 = _build_prefill(dev)
-    flops3 = sum(2 * PREFILL_M * N * K for (_, N, K) in mats3)
-    bytes3 = sum(Wd.numel() for (Wd, _, _) in mats3)
-    launches3 = len(mats3)
-    with torch.cuda.stream(stream):
-        sweep3 = _sweep_fn(q4k, mats3, x_dev3, y3, PREFILL_M, True)
-        sweep3(stream.cuda_stream)
-        torch.cuda.synchronize()
-        g3 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g3, stream=stream):
-            sweep3(torch.cuda.current_stream().cuda_stream)
-    torch.cuda.synchronize()
-    ms3 = _time_graph(torch, g3, stream, max(1, args.steps // 4), args.warmup, barrier)
-    clocks = sampler.stop()
+    if args.only in ("all", "decode"):
+        w1, mats1 = _weights(DECODE_WL, dev, args.layers)
+        Ks = sorted({K for (_, _, K) in mats1})
+        x_host = {K: synth.activations(synth.x_seed(DECODE_WL, K, 1), 1, K).pin_memory() for K in Ks}
+        x_dev = {K: x_host[K].to(dev) for K in Ks}
+        y1 = torch.empty(sum(N for (_, N, _) in mats1), device=dev)
+        calls1 = _sweep_calls(q4k, mats1, x_dev, y1, 1, False, sp)
+        g1 = _capture(torch, calls1, stream)
+        bytes1 = sum(Wd.numel() for (Wd, _, _) in mats1)
+        # steady load for ~1.5 s so that the clock samples see the working clock
+        with torch.cuda.stream(stream):
+            t_end = time.time() + 1.5
+            while time.time() < t_end:
+                for _ in range(50):
+                    g1.replay()
+                torch.cuda.synchronize()
+        times["decode"] = _time_graph(torch, g1, stream, args.steps, args.warmup, barrier)
+        launches += args.steps * len(mats1)
+        # e2e through the public API with host buffers: copy the activation rows
+        # in from pinned memory, run the captured q4k_matmul calls, read every
+        # output row back.
+        y_host = torch.empty(y1.numel(), pin_memory=True)
+        h2d = sum(x.numel() * 4 for x in x_host.values())
+        d2h = y1.numel() * 4
+        with torch.cuda.stream(stream):
+            def e2e_step():
+                for K, xh in x_host.items():
+                    x_dev[K].copy_(xh, non_blocking=True)
+                g1.replay()
+                y_host.copy_(y1, non_blocking=True)
+                stream.synchronize()
+            for _ in range(args.warmup):
+                e2e_step()
+            barrier()
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                e2e_step()
+            times["e2e"] = (time.perf_counter() - t0) * 1e3 / args.steps
+            barrier()
+        launches += args.steps * len(mats1)
+        bpl = bytes1 / len(mats1)
+        gemv_ms = times["decode"] / len(mats1)  # in-graph, gaps between launches included
+        achieved = bpl / (gemv_ms * 1e-3) / 1e9
+        out.update({
+            "unit": "GB/s",
+            "config": {"workload": f"{w1.name}: {len(mats1)} Q4_K matrices, "
+                                   f"{bytes1 / 1e6:.1f} MB packed, M=1 fp32 activations",
+                       "l2": "inputs larger than L2 (every step streams all weights from HBM)",
+                       "launch": f"one CUDA graph per sweep, q4k_set_pdl({args.pdl})",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "hbm", "kernel": "gemv_kernel<1,f32>", "achieved": round(achieved, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                         "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                         "traffic": measured_traffic("gemv_kernel<1,f32>"),
+                         "avg_launch_us": round(gemv_ms * 1e3, 3),
+                         "avg_launch_basis": "CUDA-graph sweep time / launches (gaps included)",
+                         "algorithmic_bytes_per_launch": round(bpl)},
+            "e2e": {"unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        })
+        del g1
+        out["_bytes1"] = bytes1
+        for (Wd, _, _) in mats1:
+            del Wd
+        del mats1, calls1
+        torch.cuda.empty_cache()
 
-    # ------------------------------------------- per-launch kernel durations ---
-    lib = q4k.lib()
-    with torch.cuda.stream(stream):
-        sp = stream.cuda_stream
-        calls1 = [(lambda Wd=Wd, N=N, K=K, o=o: lib.q4k_matmul(Wd.data_ptr(), N, K,
-                                                               x_dev1[K].data_ptr(), 1,
-                                                               y1.data_ptr() + 4 * o, sp))
-                  for (Wd, N, K), o in zip(mats1, _offsets(mats1))]
-        gemv_ms = _per_launch_ms(torch, calls1, stream)
-        calls3 = [(lambda Wd=Wd, N=N, K=K: lib.q4k_matmul_bf16(Wd.data_ptr(), N, K,
-                                                               x_dev3[K].data_ptr(), PREFILL_M,
-                                                               y3.data_ptr(), sp))
-                  for (Wd, N, K) in mats3]
-        gemm_ms = _per_launch_ms(torch, calls3, stream, reps=1)
+    if args.only in ("all", "prefill"):
+        w3, mats3 = _weights(PREFILL_WL, dev, args.layers)
+        Ks = sorted({K for (_, _, K) in mats3})
+        x3 = {K: synth.activations(synth.x_seed(PREFILL_WL, K, PREFILL_M), PREFILL_M, K,
+                                   torch.bfloat16).to(dev) for K in Ks}
+        y3 = torch.empty(PREFILL_M * max(N for (_, N, _) in mats3), device=dev)
+        calls3 = _sweep_calls(q4k, mats3, x3, y3, PREFILL_M, True, sp)
+        g3 = _capture(torch, calls3, stream)
+        flops3 = sum(2 * PREFILL_M * N * K for (_, N, K) in mats3)
+        bytes3 = sum(Wd.numel() for (Wd, _, _) in mats3)
+        steps3 = max(3, args.steps // 4)
+        times["prefill"] = _time_graph(torch, g3, stream, steps3, args.warmup, barrier)
+        launches += steps3 * len(mats3)
+        gemm_ms = times["prefill"] / len(mats3)  # in-graph, gaps between launches included
+        achieved3 = flops3 / len(mats3) / (gemm_ms * 1e-3) / 1e12
+        out["gemm"] = {
+            "metric": "GEMM TFLOP/s (M=512)", "unit": "TFLOP/s", "steps": steps3,
+            "workload": f"{w3.name}: {len(mats3)} Q4_K matrices, {bytes3 / 1e9:.2f} GB packed, "
+                        f"M={PREFILL_M} bf16 activations",
+            "roofline": {"bound": "tensor", "kernel": "gemm_kernel<256>",
+                         "achieved": round(achieved3, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(achieved3 / bf16_peak, 4),
+                         "frac_of_sustained": round(achieved3 / bf16_sust, 4) if bf16_sust else None,
+                         "peak_source": f"{peak_kind} bf16_tflops (cuBLAS burst)",
+                         "traffic": measured_traffic("gemm_kernel<256>"),
+                         "avg_launch_us": round(gemm_ms * 1e3, 2),
+                         "avg_launch_basis": "CUDA-graph sweep time / launches (gaps included)"}}
+        out["_flops3"] = flops3
 
-    # ------------------------------------------------------------------ e2e ---
-    # the public C ABI with host buffers: per step, copy the activation rows
-    # from pinned host memory, run the sweep, read all outputs back.
-    y_host = torch.empty(y1.numel(), pin_memory=True)
-    h2d = sum(x.numel() * 4 for x in x_host1.values())
-    d2h = y1.numel() * 4
-    with torch.cuda.stream(stream):
-        def e2e_step():
-            for K, xh in x_host1.items():
-                x_dev1[K].copy_(xh, non_blocking=True)
-            sweep1(stream.cuda_stream)
-            y_host.copy_(y1, non_blocking=True)
-        for _ in range(args.warmup):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        torch.cuda.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-        barrier()
-
-    # ------------------------------------------------------- max over ranks ---
-    times = torch.tensor([ms1, ms3, e2e_ms], device=dev, dtype=torch.float64)
+    out["clocks"] = sampler.stop()
+    # max over ranks
+    keys = sorted(times)
+    t = torch.tensor([times[k] for k in keys], device=dev, dtype=torch.float64)
     if ws > 1:
         import torch.distributed as dist
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms1, ms3, e2e_ms = times.tolist()
-    err = q4k.q4k_device_error()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    times = dict(zip(keys, t.tolist()))
+    out["device_error"] = q4k.q4k_device_error()
+    out["gpu_launches"] = launches
     if rank != 0:
         return
-    value = ws * bytes1 / (ms1 * 1e-3) / 1e9
-    gemm_tflops = ws * flops3 / (ms3 * 1e-3) / 1e12
-    gemv_bytes_per_launch = bytes1 / launches1
-    gemv_achieved = gemv_bytes_per_launch / (gemv_ms * 1e-3) / 1e9
-    gemm_achieved = flops3 / launches3 / (gemm_ms * 1e-3) / 1e12
-    out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms1, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded Q4_K weights, N(0,1) activations)",
-        "config": {"workload": f"{w1.name}: {launches1} Q4_K matrices, "
-                               f"{bytes1 / 1e6:.1f} MB packed, M=1 fp32 activations",
-                   "l2": "inputs larger than L2 (every step streams all weights from HBM)",
-                   "launch": "one CUDA graph per sweep", "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<1,f32>",
-                     "achieved": round(gemv_achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(gemv_achieved / hbm, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": None,
-                     "avg_launch_us": round(gemv_ms * 1e3, 3),
-                     "algorithmic_bytes_per_launch": round(gemv_bytes_per_launch)},
-        "gemm": {"metric": "GEMM TFLOP/s (M=512)", "value": round(gemm_tflops, 2), "unit": "TFLOP/s",
-                 "workload": f"{w3.name}: {launches3} Q4_K matrices, {bytes3 / 1e9:.2f} GB packed, "
-                             f"M={PREFILL_M} bf16 activations",
-                 "ms_per_step": round(ms3, 4), "steps": max(1, args.steps // 4),
-                 "roofline": {"bound": "tensor", "kernel": "gemm_kernel<256>",
-                              "achieved": round(gemm_achieved, 1), "peak": bf16_peak,
-                              "unit": "TFLOP/s", "frac": round(gemm_achieved / bf16_peak, 4),
-                              "frac_of_sustained": (round(gemm_achieved / bf16_sust, 4)
-                                                    if bf16_sust else None),
-                              "peak_source": f"{peak_kind} bf16_tflops", "traffic": None,
-                              "avg_launch_us": round(gemm_ms * 1e3, 2)}},
-        "e2e": {"value": round(ws * bytes1 / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": args.steps * launches1 + max(1, args.steps // 4) * launches3,
-        "clocks": clocks,
-        "device_error": err,
-    }
-    if ws == 1 and not args.no_cpu_baseline:
+    if "decode" in times:
+        b1 = out.pop("_bytes1")
+        out["value"] = round(ws * b1 / (times["decode"] * 1e-3) / 1e9, 2)
+        out["ms_per_step"] = round(times["decode"], 5)
+        out["e2e"]["value"] = round(ws * b1 / (times["e2e"] * 1e-3) / 1e9, 2)
+        out["e2e"]["ms_per_step"] = round(times["e2e"], 4)
+    if "prefill" in times:
+        f3 = out.pop("_flops3")
+        out["gemm"]["value"] = round(ws * f3 / (times["prefill"] * 1e-3) / 1e12, 2)
+        out["gemm"]["ms_per_step"] = round(times["prefill"], 4)
+    if args.layers:
+        out["config"] = dict(out.get("config", {}), profiling_subset=f"first {args.layers} layers")
+    if ws == 1 and not args.no_cpu_baseline and args.only == "all":
         out["cpu_baseline"] = cpu_oracle_decode(args.cpu_budget, _host_cores())
     print(json.dumps(out))
-
-
-def _offsets(mats):
-    o, offs = 0, []
-    for (_, N, _) in mats:
-        offs.append(o)
-        o += N
-    return offs
 
 
 def main():
@@ -416,11 +460,23 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=5.0,
                     help="seconds of oracle CPU time per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pdl", type=int, default=2, choices=[0, 1, 2],
+                    help="q4k_set_pdl mode for the sweeps (2: weights may stream early)")
+    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill"],
+                    help="profiling aid: run one leg only")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: use only the first L layers of each weight set")
+    ap.add_argument("--profile-shape", default="",
+                    help="microbenchmark one shape 'N,K,M' (bf16 activations when M > 16)")
+    ap.add_argument("--profile-bytes", type=float, default=300e6,
+                    help="weight bytes to rotate through in --profile-shape (> L2)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.profile_shape:
+        run_profile_shape(args)
     else:
         run_gpu(args)
 

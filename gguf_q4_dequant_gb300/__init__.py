@@ -25,7 +25,7 @@ Q4K_ERR_TIMEOUT = -6
 
 #: every symbol include/q4k.h declares
 EXPORTS = ("q4k_status_string", "q4k_init", "q4k_dequant", "q4k_matmul", "q4k_matmul_bf16",
-           "q4k_device_error")
+           "q4k_set_pdl", "q4k_device_error")
 
 
 _STATUS_NAMES = {Q4K_OK: "Q4K_OK", Q4K_ERR_NULL: "Q4K_ERR_NULL", Q4K_ERR_BAD_DIM: "Q4K_ERR_BAD_DIM",
@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.q4k_matmul.restype = ctypes.c_int
             L.q4k_matmul_bf16.argtypes = [vp, i64, i64, vp, i64, vp, vp]
             L.q4k_matmul_bf16.restype = ctypes.c_int
+            L.q4k_set_pdl.argtypes = [ctypes.c_int]
+            L.q4k_set_pdl.restype = ctypes.c_int
             L.q4k_device_error.argtypes = [ctypes.c_int]
             L.q4k_device_error.restype = ctypes.c_int
             _lib = L
@@ -133,6 +135,14 @@ def q4k_matmul_bf16(W, N: int, K: int, X, M: int, Y, stream=None):
     _check_dtype(Y, torch.float32, "Y")
     _check(lib().q4k_matmul_bf16(_ptr(W), N, K, _ptr(X), M, _ptr(Y), _stream(stream)),
            "q4k_matmul_bf16")
+
+
+def q4k_set_pdl(mode: int) -> int:
+    """Programmatic-dependent-launch mode for later calls (0, 1 or 2); returns the old mode."""
+    rc = lib().q4k_set_pdl(int(mode))
+    if rc < 0:
+        raise Q4KError(rc, "q4k_set_pdl")
+    return rc
 
 
 def q4k_device_error(clear: bool = True) -> int:

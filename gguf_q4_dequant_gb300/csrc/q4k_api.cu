@@ -11,9 +11,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
-#include "../../include/q4k.h"
+#include "q4k.h"
 #include "q4k_internal.h"
 
 namespace q4k {
@@ -33,6 +34,7 @@ struct DeviceState {
 };
 
 DeviceState g_dev[kMaxDevices];
+std::atomic<int> g_pdl{0};  // q4k_set_pdl mode
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -123,14 +125,14 @@ int encode_x_bf16(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN)
 int run_gemv(const void* W, int64_t N, int64_t K, const void* X, bool xb, int64_t M, float* Y,
              cudaStream_t stream, const DeviceInfo& dev) {
     CUtensorMap tw;
-    int rc = encode_w(&tw, W, N, K, 32);
+    int rc = encode_w(&tw, W, N, K, 128);
     if (rc != Q4K_OK) return rc;
     const size_t xelem = xb ? 2 : 4;
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mc = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
         const void* Xc = static_cast<const uint8_t*>(X) + static_cast<size_t>(m0) * K * xelem;
         if (launch_gemv(tw, Xc, xb, mc, static_cast<int>(N), static_cast<int>(K), Y + m0 * N, stream,
-                        dev) != cudaSuccess)
+                        dev, g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
             return Q4K_ERR_CUDA;
     }
     return Q4K_OK;
@@ -202,9 +204,14 @@ int q4k_matmul_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16,
     if ((rc = encode_w(&tw, W, N, K, 128)) != Q4K_OK) return rc;
     if ((rc = encode_x_bf16(&tx, X_bf16, M, K, BN)) != Q4K_OK) return rc;
     if (launch_gemm(tw, tx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), Y, BN, st,
-                    *dev) != cudaSuccess)
+                    *dev, g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
         return Q4K_ERR_CUDA;
     return Q4K_OK;
+}
+
+int q4k_set_pdl(int mode) {
+    if (mode < 0 || mode > 2) return Q4K_ERR_BAD_DIM;
+    return g_pdl.exchange(mode);
 }
 
 int q4k_device_error(int clear) {

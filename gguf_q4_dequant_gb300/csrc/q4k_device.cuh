@@ -140,11 +140,43 @@ __device__ __forceinline__ ScaleBytes decode_scales(uint32_t s0, uint32_t s1, ui
 
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int i) { return (w >> (8 * i)) & 0xFFu; }
 
+// Byte i of w as a float: one byte permute builds 2^23 + byte exactly
+// (0x4B0000bb), one FP subtraction removes 2^23.
+__device__ __forceinline__ float byte_to_float(uint32_t w, int i) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | static_cast<uint32_t>(i))) - 8388608.f;
+}
+
 __device__ __forceinline__ float half_lo(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
 }
 __device__ __forceinline__ float half_hi(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// Packed fp32 pairs for the sm_100+ paired FMA: element 0 in the low half.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+// d = a * b + c, elementwise on fp32 pairs, each lane rounded to nearest even
+// (subnormal operands are kept: no .ftz).
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// a + b elementwise on fp32 pairs.
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
 // 2^n as a float for n in [-126, 127].
@@ -252,6 +284,17 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+
+// Programmatic dependent launch. Both are no-ops unless the kernel was launched
+// with programmatic stream serialisation.
+//   pdl_wait(): wait until the preceding grid on the stream has completed and
+//               its memory operations are visible.
+//   pdl_launch_dependents(): allow the next grid on the stream to start
+//               launching (it still waits in its own pdl_wait()).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads).

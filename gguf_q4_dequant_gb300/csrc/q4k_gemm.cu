@@ -72,7 +72,7 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, int shift, f
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ CUtensorMap tmapX,
-                int M, int N, int K, float* __restrict__ Y, unsigned int* err) {
+                int M, int N, int K, float* __restrict__ Y, int pdl_flags, unsigned int* err) {
     using Cfg = GemmCfg<BN>;
     constexpr int S = Cfg::kABStages;
     extern __shared__ uint8_t smem_raw[];
@@ -116,6 +116,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    // Every warp except the producer waits for the preceding grid here; the
+    // producer waits before its first activation load (and, unless weight
+    // prefetch is allowed, before its first weight load).
+    if (warp != 0) pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ---
@@ -124,6 +129,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tma_prefetch_desc(&tmapX);
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
+            if (pdl_flags & 1) pdl_wait();
             for (int ks = 0; ks < nks; ++ks) {
                 if ((ks & 3) == 0) {
                     const int sb = ks >> 2;
@@ -135,6 +141,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 const int s = ks % S;
                 if (!mbar_wait(bab_empty + 8 * s, ((ks / S) & 1) ^ 1, err)) break;
+                if (ks == 0 && !(pdl_flags & 1)) pdl_wait();
                 mbar_arrive_expect_tx(bb_full + 8 * s, Cfg::kBStageBytes);
                 tma_load_2d_hint(sbase + Cfg::kOffB + s * Cfg::kBStageBytes, &tmapX, ks * kGemmKStep,
                                  m0, bb_full + 8 * s, pol_x);
@@ -256,19 +263,30 @@ cudaError_t gemm_setup() {
 
 template <int BN>
 static cudaError_t launch_bn(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                             float* Y, cudaStream_t stream, unsigned int* err) {
-    dim3 grid((N + kGemmBM - 1) / kGemmBM, (M + BN - 1) / BN, 1);
-    gemm_kernel<BN><<<grid, kGemmThreads, GemmCfg<BN>::kSmem, stream>>>(tmapW, tmapX, M, N, K, Y, err);
-    return cudaGetLastError();
+                             float* Y, cudaStream_t stream, unsigned int* err, int pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + kGemmBM - 1) / kGemmBM, (M + BN - 1) / BN, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = GemmCfg<BN>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    const int pdl_flags = (pdl == 2) ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, tmapW, tmapX, M, N, K, Y, pdl_flags, err);
 }
 
 cudaError_t launch_gemm(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                        float* Y, int BN, cudaStream_t stream, const DeviceInfo& dev) {
+                        float* Y, int BN, cudaStream_t stream, const DeviceInfo& dev, int pdl) {
     switch (BN) {
-        case 32: return launch_bn<32>(tmapW, tmapX, M, N, K, Y, stream, dev.err);
-        case 64: return launch_bn<64>(tmapW, tmapX, M, N, K, Y, stream, dev.err);
-        case 128: return launch_bn<128>(tmapW, tmapX, M, N, K, Y, stream, dev.err);
-        case 256: return launch_bn<256>(tmapW, tmapX, M, N, K, Y, stream, dev.err);
+        case 32: return launch_bn<32>(tmapW, tmapX, M, N, K, Y, stream, dev.err, pdl);
+        case 64: return launch_bn<64>(tmapW, tmapX, M, N, K, Y, stream, dev.err, pdl);
+        case 128: return launch_bn<128>(tmapW, tmapX, M, N, K, Y, stream, dev.err, pdl);
+        case 256: return launch_bn<256>(tmapW, tmapX, M, N, K, Y, stream, dev.err, pdl);
     }
     return cudaErrorInvalidValue;
 }

@@ -5,45 +5,66 @@
 // HBM bandwidth at M = 1 and by fp32 issue rate as M grows.
 //
 // Work decomposition
-//   grid.x  = 32-row groups of W (one warp lane per weight row)
-//   grid.y  = K splits (a thread-block cluster along y; partial sums are
-//             reduced through distributed shared memory, in rank order)
-//   CTA     = 4 consumer warps that split the CTA's super-blocks between them,
-//             plus one producer warp that streams the packed tiles with TMA.
-// A TMA box is {144 bytes, 32 rows}: one super-block of 32 consecutive rows,
-// landing in shared memory as [row][144] so that the 32 lanes' 16-byte loads
-// of one super-block hit distinct banks.
+//   tile      = 128 consecutive rows of W; one TMA box {144 bytes, 128 rows}
+//               brings one super-block of every row of the tile into shared
+//               memory as [row][144] (a stage, 18 KB).
+//   K-slice   = a contiguous range of super-blocks. When there are fewer tiles
+//               than CTA slots, the K range is split across a thread-block
+//               cluster (one K-slice per CTA) and the partial sums are reduced
+//               once, in rank order, through distributed shared memory.
+//   CTA       = 8 consumer warps in two groups of 4 (warp w of a group owns
+//               rows 32w..32w+31 of the tile, one lane per row; the groups take
+//               alternate stages and add their sums once per tile), 1 TMA
+//               producer warp, 1 activation warp. CTAs are persistent over
+//               tiles, so the stage ring streams continuously.
 //
 // Per-weight arithmetic (the unpack happens in registers):
-//   A 4-bit quant q left in place inside its 32-bit word at bit 4p (p = 0..3)
+//   A 4-bit quant q left in place inside its 32-bit word at bit 4p (p = 0..4)
 //   is, read as an fp32 bit pattern, the subnormal q * 2^(4p-149); the fp32
-//   FMA handles subnormal operands at full rate without flushing. Each
-//   activation is pre-scaled once per (block, row of X) by 2^(E+149-4p), so
-//   one mask and one FMA give q*x*2^E exactly rounded, with no int->float
-//   conversion. E is chosen from the block's largest |x| so that neither the
-//   scaled activations overflow nor the products leave the normal range.
-//   Sub-block sums are then combined as d*sc*S - dmin*m*sum(x) and rescaled.
+//   FMA handles subnormal operands at full rate without flushing. Two
+//   neighbouring qs words form one 64-bit register pair, so a 64-bit mask
+//   yields the same nibble of both words as an fp32 pair for the paired FMA
+//   (fma.rn.f32x2); the top three nibbles of each word are first brought down
+//   by one 64-bit shift by 12. Each activation is pre-scaled once per
+//   (super-block, row of X) by 2^(E+149-4p) by the activation warp and stored
+//   in the order the pairs consume them, so a mask and half a paired FMA per
+//   weight give q*x*2^E with a single rounding and no int->float conversion.
+//   E is chosen from the block's largest |x| so that neither the scaled
+//   activations overflow nor the products leave the normal range. Sub-block
+//   sums are then combined as d*sc*S - dmin*m*sum(x) and scaled back by 2^-E.
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
 
 namespace q4k {
 
-constexpr int kGemvConsumers = 4;
-constexpr int kGemvThreads = 32 * (kGemvConsumers + 1);
-constexpr int kGemvRows = 32;
-constexpr int kGemvSubBytes = kGemvRows * kBlockBytes;               // 4608
-constexpr int kGemvStageBytes = kGemvConsumers * kGemvSubBytes;      // 18432
+constexpr int kGemvTileRows = 128;
+constexpr int kGemvGroupWarps = 4;     // one consumer group covers the 128-row tile
+constexpr int kGemvStageBytes = kGemvTileRows * kBlockBytes;  // 18432
 
 template <int MT>
 struct GemvCfg {
-    static constexpr int kStages = MT >= 8 ? 2 : 3;
+    // two consumer groups (alternate stages) for small M; one group for
+    // M >= 8, whose register footprint leaves no room for a second
+    static constexpr int kGroups = MT >= 8 ? 1 : 2;
+    static constexpr int kConsumers = kGroups * kGemvGroupWarps;
+    static constexpr int kProducerWarp = kConsumers;
+    static constexpr int kStagerWarp = kConsumers + 1;
+    static constexpr int kThreads = 32 * (kConsumers + 2);
+    // registers: two resident CTAs per SM for small M (measured: more registers
+    // per thread buy more overlap than a third CTA would); M >= 8 needs ~250
+    static constexpr int kMinBlocks = MT >= 8 ? 1 : 2;
+    // Even, so that slot s is only ever used by consumer group s % 2 (a group
+    // takes the stages of its parity); a group therefore never waits on a
+    // slot more than one phase ahead of it.
+    static constexpr int kStages = 4;
     static constexpr int kOffW = 0;
-    static constexpr int kOffX = kOffW + kStages * kGemvStageBytes;              // x' [warp][m][256]
-    static constexpr int kOffXs = kOffX + kGemvConsumers * MT * 256 * 4;          // sums [warp][m][8]
-    static constexpr int kOffRed = kOffXs + kGemvConsumers * MT * 8 * 4;          // [warp][m][32]
-    static constexpr int kOffPart = kOffRed + kGemvConsumers * MT * 32 * 4;       // [m][32]
-    static constexpr int kOffBar = kOffPart + MT * 32 * 4;                        // full, empty
-    static constexpr int kSmem = kOffBar + 2 * kStages * 8 + 128;  // + alignment slack
+    static constexpr int kOffX = kOffW + kStages * kGemvStageBytes;     // x' [stage][m][256]
+    static constexpr int kOffXs = kOffX + kStages * MT * 256 * 4;        // sums [stage][m][8]
+    static constexpr int kOffInv = kOffXs + kStages * MT * 8 * 4;        // 2^-E [stage][m][2]
+    static constexpr int kOffPart = kOffInv + kStages * MT * 2 * 4;      // cluster partials [m][128]
+    static constexpr int kOffGrp = kOffPart + MT * kGemvTileRows * 4;    // group-1 sums [2][m][128]
+    static constexpr int kOffBar = kOffGrp + 2 * MT * kGemvTileRows * 4; // full[S], empty[S]
+    static constexpr int kSmem = kOffBar + 2 * kStages * 8 + 128;        // + alignment slack
 };
 
 // Loads 8 consecutive activations of row m as fp32 (zeros past M).
@@ -79,214 +100,307 @@ __device__ __forceinline__ int block_exponent(float amax) {
     return e < -20 ? -20 : (e > 127 ? 127 : e);
 }
 
+// Pre-scales one row of activations for the subnormal-quant products and
+// stores it in consumption order. Lane l holds x for k = 8l .. 8l+7 of the
+// super-block: chunk c = l/8, high-nibble half h = (l/4)%2, word pair v = l%4,
+// element i = 4*up + j (up: which word of the pair, j: byte in the word).
+// The consumer reads, per word pair, 16 floats ordered
+//   [A A C C E E G G | B B D D F F H H]   (each letter: word u, word u+1)
+// where A,C,E,G are the low nibbles of bytes 0..3 and B,D,F,H the high ones,
+// so this lane's 8 values go to the 8 floats at c*64 + v*16 + 8h, slot 2j+up.
+// The nibble positions p (value q*2^(4p-149)) are A0 C2 E4 G3 and B1 D3 F2 H4.
+// Also stores the sub-block sums scaled by 2^E and 2^-E (as two factors).
+__device__ __forceinline__ void scale_activations(const float (&v)[8], int lane, float* xs,
+                                                  float* xsum, float* inv) {
+    const int h = (lane >> 2) & 1;
+    uint32_t amax = 0;  // |x| bit patterns order like the values
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        sum += v[i];
+    }
+    amax = __reduce_max_sync(~0u, amax);
+    sum += __shfl_xor_sync(~0u, sum, 1);
+    sum += __shfl_xor_sync(~0u, sum, 2);
+    const int e = block_exponent(__uint_as_float(amax));
+    // E = -23 - e; x' = x * 2^(E + 149 - 4p) = x * 2^(126 - e - 4p)
+    const int base = 126 - e;
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        // nibble position of byte j's low (h = 0) or high (h = 1) nibble
+        const int p = h ? ((0x4231 >> (4 * j)) & 0xF) : ((0x3420 >> (4 * j)) & 0xF);
+        const int t = base - 4 * p;
+        const float fa = exp2i(t >> 1), fb = exp2i(t - (t >> 1));
+        o[2 * j] = (v[j] * fa) * fb;          // up = 0: word u
+        o[2 * j + 1] = (v[4 + j] * fa) * fb;  // up = 1: word u+1
+    }
+    float4* dst = reinterpret_cast<float4*>(xs + (lane >> 3) * 64 + (lane & 3) * 16 + 8 * h);
+    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    const int E = -23 - e;
+    if ((lane & 3) == 0) xsum[lane >> 2] = (sum * exp2i(E >> 1)) * exp2i(E - (E >> 1));
+    if (lane == 0) {
+        const int ie = 23 + e;
+        inv[0] = exp2i(ie >> 1);
+        inv[1] = exp2i(ie - (ie >> 1));
+    }
+}
+
+// Rows kept in registers across one stage by the activation warp (the next
+// stage's loads are in flight while the current stage is written): all of
+// them for small M, none (load-and-use) for M >= 8 where the consumers are
+// compute-bound anyway.
+template <int MT>
+struct XPrefetch {
+    static constexpr int kRows = MT <= 4 ? MT : 0;
+};
+// One consumer lane: the contribution of one super-block of its row, scaled by
+// 2^E (acc[m] for each activation row m).
+template <int MT>
+__device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, const float* xsum,
+                                          float (&acc)[MT]) {
+    const uint4 h = *reinterpret_cast<const uint4*>(P);
+    const ScaleBytes sb = decode_scales(h.y, h.z, h.w);
+    const float d = half_lo(h.x), dmin = half_hi(h.x);
+    uint64_t dsc[8];  // (d*sc_j, d*sc_j) pairs
+    float mm[8];      // dmin*m_j
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float a = d * byte_to_float(sb.sc_lo, j), b = d * byte_to_float(sb.sc_hi, j);
+        dsc[j] = pack2(a, a);
+        dsc[j + 4] = pack2(b, b);
+        mm[j] = dmin * byte_to_float(sb.m_lo, j);
+        mm[j + 4] = dmin * byte_to_float(sb.m_hi, j);
+    }
+    uint64_t tot[MT];  // sum over sub-blocks of d*sc_j*S_j, as a pair
+#pragma unroll
+    for (int m = 0; m < MT; ++m) tot[m] = 0ull;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        // the 32 qs bytes of chunk c as four word pairs (u, u+1)
+        const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c);
+        const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(P + 32 + 32 * c);
+        const uint64_t wp[4] = {qa.x, qa.y, qb.x, qb.y};
+        uint64_t lo_a[MT], lo_b[MT], hi_a[MT], hi_b[MT];  // fp32 pair accumulators
+#pragma unroll
+        for (int m = 0; m < MT; ++m) lo_a[m] = lo_b[m] = hi_a[m] = hi_b[m] = 0ull;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint64_t Pw = wp[v];
+            const uint64_t Sw = Pw >> 12;  // bytes 2 (high nibble) and 3 of each word, brought down
+            const uint64_t qA = Pw & 0x0000000F0000000Full;  // byte 0 low   p0
+            const uint64_t qB = Pw & 0x000000F0000000F0ull;  // byte 0 high  p1
+            const uint64_t qC = Pw & 0x00000F0000000F00ull;  // byte 1 low   p2
+            const uint64_t qD = Pw & 0x0000F0000000F000ull;  // byte 1 high  p3
+            const uint64_t qE = Pw & 0x000F0000000F0000ull;  // byte 2 low   p4
+            const uint64_t qF = Sw & 0x00000F0000000F00ull;  // byte 2 high  p2
+            const uint64_t qG = Sw & 0x0000F0000000F000ull;  // byte 3 low   p3
+            const uint64_t qH = Sw & 0x000F0000000F0000ull;  // byte 3 high  p4
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const ulonglong2* xp = reinterpret_cast<const ulonglong2*>(xs + m * 256 + 64 * c + 16 * v);
+                const ulonglong2 x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
+                lo_a[m] = fma2(qA, x0.x, lo_a[m]);
+                lo_b[m] = fma2(qC, x0.y, lo_b[m]);
+                lo_a[m] = fma2(qE, x1.x, lo_a[m]);
+                lo_b[m] = fma2(qG, x1.y, lo_b[m]);
+                hi_a[m] = fma2(qB, x2.x, hi_a[m]);
+                hi_b[m] = fma2(qD, x2.y, hi_b[m]);
+                hi_a[m] = fma2(qF, x3.x, hi_a[m]);
+                hi_b[m] = fma2(qH, x3.y, hi_b[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            tot[m] = fma2(add2(lo_a[m], lo_b[m]), dsc[2 * c], tot[m]);
+            tot[m] = fma2(add2(hi_a[m], hi_b[m]), dsc[2 * c + 1], tot[m]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const float* xsm = xsum + m * 8;
+        float mins = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mins = fmaf(mm[j], xsm[j], mins);
+        const float2 t = unpack2(tot[m]);
+        acc[m] = (t.x + t.y) - mins;
+    }
+}
+
+// Grid: gridDim.x = (number of clusters) * C; a cluster of C CTAs along x
+// shares tiles and splits K into C slices of kb_per super-blocks. With C > 1
+// every cluster owns exactly one tile.
 template <int MT, bool XB>
-__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constant__ CUtensorMap tmapW,
-                                                            const void* __restrict__ X, int M, int N,
-                                                            int K, float* __restrict__ Y,
-                                                            int kb_per_split, unsigned int* err) {
+__global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks)
+    gemv_kernel(const __grid_constant__ CUtensorMap tmapW, const void* __restrict__ X, int M, int N,
+                int K, float* __restrict__ Y, int tiles, int C, int kb_per, int pdl_flags,
+                unsigned int* err) {
     using Cfg = GemvCfg<MT>;
-    constexpr int NS = Cfg::kStages;
+    constexpr int S = Cfg::kStages;
+    static_assert(S % Cfg::kGroups == 0, "slot s must belong to consumer group s % G");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = K / kBlockWeights;
-    const int row0 = blockIdx.x * kGemvRows;
-    const int kb0 = blockIdx.y * kb_per_split;
-    const int kb1 = min(KB, kb0 + kb_per_split);
-    const int nst = (kb1 - kb0 + kGemvConsumers - 1) / kGemvConsumers;  // stages for this CTA
+    const int rank = blockIdx.x % C;
+    const int cid = blockIdx.x / C;
+    const int ncl = gridDim.x / C;
+    const int kb0 = rank * kb_per;
+    const int nb = min(KB, kb0 + kb_per) - kb0;
+    const int nt_local = (tiles - cid + ncl - 1) / ncl;  // tiles cid, cid + ncl, ...
+    const int total = nt_local * nb;                     // stages this CTA streams
 
-    const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + Cfg::kOffBar;
-    const uint32_t bar_empty = bar_full + NS * 8;
-    float* xs_all = reinterpret_cast<float*>(smem + Cfg::kOffX);
-    float* xsum_all = reinterpret_cast<float*>(smem + Cfg::kOffXs);
-    float* red = reinterpret_cast<float*>(smem + Cfg::kOffRed);
+    const uint32_t bar_empty = bar_full + 8 * S;
+    float* xs_ring = reinterpret_cast<float*>(smem + Cfg::kOffX);
+    float* xsum_ring = reinterpret_cast<float*>(smem + Cfg::kOffXs);
+    float* inv_ring = reinterpret_cast<float*>(smem + Cfg::kOffInv);
     float* part = reinterpret_cast<float*>(smem + Cfg::kOffPart);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, kGemvConsumers);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8 * s, 1 + 32);  // producer (with bytes) + 32 activation lanes
+            mbar_init(bar_empty + 8 * s, kGemvGroupWarps);  // one group consumes a stage
         }
         fence_barrier_init();
     }
     __syncthreads();
+    if (threadIdx.x == 0) pdl_launch_dependents();
 
-    if (warp == kGemvConsumers) {
-        // ------------------------------------------------ TMA producer ---
+    if (warp == Cfg::kProducerWarp) {
+        // ---------------------------------------------------- TMA producer ---
         if (lane == 0) {
             tma_prefetch_desc(&tmapW);
+            if (pdl_flags & 1) pdl_wait();
             const uint64_t pol = policy_evict_first();
-            for (int st = 0; st < nst; ++st) {
-                const int s = st % NS;
-                const uint32_t ph = (st / NS) & 1;
-                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, err)) break;
-                const int b0 = kb0 + st * kGemvConsumers;
-                const int nb = min(kGemvConsumers, kb1 - b0);
-                mbar_arrive_expect_tx(bar_full + 8 * s, nb * kGemvSubBytes);
-                for (int i = 0; i < nb; ++i)
-                    tma_load_2d_hint(sbase + Cfg::kOffW + s * kGemvStageBytes + i * kGemvSubBytes,
-                                     &tmapW, (b0 + i) * kBlockBytes, row0, bar_full + 8 * s, pol);
+            for (int st = 0; st < total; ++st) {
+                const int s = st % S;
+                if (!mbar_wait(bar_empty + 8 * s, ((st / S) & 1) ^ 1, err)) break;
+                const int t = cid + (st / nb) * ncl;
+                const int b = kb0 + st % nb;
+                mbar_arrive_expect_tx(bar_full + 8 * s, kGemvStageBytes);
+                tma_load_2d_hint(sbase + Cfg::kOffW + s * kGemvStageBytes, &tmapW, b * kBlockBytes,
+                                 t * kGemvTileRows, bar_full + 8 * s, pol);
             }
+            // the CTA must not exit while a copy into its shared memory is in flight
+            for (int st = total - S < 0 ? 0 : total - S; st < total; ++st)
+                mbar_wait(bar_full + 8 * (st % S), (st / S) & 1, err);
         }
         __syncwarp();
-    } else {
-        // --------------------------------------------------- consumers ---
-        float y[MT];
+    } else if (warp == Cfg::kStagerWarp) {
+        // ------------------------------------------------ activation warp ---
+        pdl_wait();
+        constexpr int PF = XPrefetch<MT>::kRows;
+        float nxt[PF > 0 ? PF : 1][8];
+        if constexpr (PF > 0) {
+            if (total > 0) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m) y[m] = 0.f;
-        float* xs = xs_all + warp * MT * 256;
-        float* xsum = xsum_all + warp * MT * 8;
-        bool ok = true;
-
-        for (int st = 0; st < nst && ok; ++st) {
-            const int s = st % NS;
-            const uint32_t ph = (st / NS) & 1;
-            const int b = kb0 + st * kGemvConsumers + warp;
-            const bool has = b < kb1;
-            float inv_a[MT], inv_b[MT];  // 2^-E as two factors
-            if (has) {
-                // stage this block's activations: lane owns k = 8*lane .. 8*lane+7
-                const int64_t kx = static_cast<int64_t>(b) * kBlockWeights + 8 * lane;
-                const int hsel = (lane >> 2) & 1;  // weight is a high-nibble one (k % 64 >= 32)
+                for (int m = 0; m < PF; ++m)
+                    load_x8<XB>(X, m, M, K, static_cast<int64_t>(kb0) * kBlockWeights + 8 * lane, nxt[m]);
+            }
+        }
+        for (int st = 0; st < total; ++st) {
+            const int s = st % S;
+            float* xs = xs_ring + s * MT * 256;
+            float* xsum = xsum_ring + s * MT * 8;
+            float* inv = inv_ring + s * MT * 2;
+            if constexpr (PF > 0) {
+                float cur[PF][8];
+#pragma unroll
+                for (int m = 0; m < PF; ++m)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) cur[m][i] = nxt[m][i];
+                if (st + 1 < total) {
+                    const int64_t kn = static_cast<int64_t>(kb0 + (st + 1) % nb) * kBlockWeights + 8 * lane;
+#pragma unroll
+                    for (int m = 0; m < PF; ++m) load_x8<XB>(X, m, M, K, kn, nxt[m]);
+                }
+                if (!mbar_wait(bar_empty + 8 * s, ((st / S) & 1) ^ 1, err)) break;
+#pragma unroll
+                for (int m = 0; m < PF; ++m)
+                    scale_activations(cur[m], lane, xs + m * 256, xsum + m * 8, inv + 2 * m);
+            } else {
+                if (!mbar_wait(bar_empty + 8 * s, ((st / S) & 1) ^ 1, err)) break;
+                const int64_t kx = static_cast<int64_t>(kb0 + st % nb) * kBlockWeights + 8 * lane;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     float v[8];
                     load_x8<XB>(X, m, M, K, kx, v);
-                    float amax = 0.f, sum = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        amax = fmaxf(amax, fabsf(v[i]));
-                        sum += v[i];
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
-                    sum += __shfl_xor_sync(~0u, sum, 1);
-                    sum += __shfl_xor_sync(~0u, sum, 2);
-                    const int e = block_exponent(amax);
-                    // E = -23 - e; x' = x * 2^(E + 149 - 4p) = x * 2^(126 - e - 4p)
-                    const int t0 = 126 - e - 4 * hsel;  // p = 2*(k&1) + hsel; even k: p = hsel
-                    const int t1 = t0 - 8;              // odd k: p = 2 + hsel
-                    const float f0a = exp2i(t0 >> 1), f0b = exp2i(t0 - (t0 >> 1));
-                    const float f1a = exp2i(t1 >> 1), f1b = exp2i(t1 - (t1 >> 1));
-                    float4 o0, o1;
-                    o0.x = (v[0] * f0a) * f0b; o0.y = (v[1] * f1a) * f1b;
-                    o0.z = (v[2] * f0a) * f0b; o0.w = (v[3] * f1a) * f1b;
-                    o1.x = (v[4] * f0a) * f0b; o1.y = (v[5] * f1a) * f1b;
-                    o1.z = (v[6] * f0a) * f0b; o1.w = (v[7] * f1a) * f1b;
-                    float4* dst = reinterpret_cast<float4*>(xs + m * 256 + 8 * lane);
-                    dst[0] = o0;
-                    dst[1] = o1;
-                    // sub-block sum scaled by 2^E, E = -23 - e (two factors)
-                    const int E = -23 - e;
-                    if ((lane & 3) == 0)
-                        xsum[m * 8 + (lane >> 2)] = (sum * exp2i(E >> 1)) * exp2i(E - (E >> 1));
-                    const int ie = 23 + e;  // 2^-E
-                    inv_a[m] = exp2i(ie >> 1);
-                    inv_b[m] = exp2i(ie - (ie >> 1));
+                    scale_activations(v, lane, xs + m * 256, xsum + m * 8, inv + 2 * m);
                 }
-                __syncwarp();
-            }
-            if (!mbar_wait(bar_full + 8 * s, ph, err)) ok = false;
-            if (has && ok) {
-                const uint8_t* P = smem + Cfg::kOffW + s * kGemvStageBytes + warp * kGemvSubBytes +
-                                   lane * kBlockBytes;
-                const uint4 h = *reinterpret_cast<const uint4*>(P);
-                const ScaleBytes sb = decode_scales(h.y, h.z, h.w);
-                const float d = half_lo(h.x), dmin = half_hi(h.x);
-                float d1[8], mm[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    d1[j] = d * static_cast<float>(byte_of(sb.sc_lo, j));
-                    mm[j] = dmin * static_cast<float>(byte_of(sb.m_lo, j));
-                    d1[j + 4] = d * static_cast<float>(byte_of(sb.sc_hi, j));
-                    mm[j + 4] = dmin * static_cast<float>(byte_of(sb.m_hi, j));
-                }
-                float acc[MT];
-#pragma unroll
-                for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 qa = *reinterpret_cast<const uint4*>(P + 16 + 32 * c);
-                    const uint4 qb = *reinterpret_cast<const uint4*>(P + 32 + 32 * c);
-                    const uint32_t wq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-                    float slo[MT], shi[MT], slo2[MT], shi2[MT];
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) slo[m] = shi[m] = slo2[m] = shi2[m] = 0.f;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t wd = wq[u], wh = wd >> 16;
-                        // low nibbles: weights 64c+4u+{0,1,2,3}; high: +32
-                        const float qA = __uint_as_float(wd & 0x000Fu);
-                        const float qC = __uint_as_float(wd & 0x0F00u);
-                        const float qE = __uint_as_float(wh & 0x000Fu);
-                        const float qG = __uint_as_float(wh & 0x0F00u);
-                        const float qB = __uint_as_float(wd & 0x00F0u);
-                        const float qD = __uint_as_float(wd & 0xF000u);
-                        const float qF = __uint_as_float(wh & 0x00F0u);
-                        const float qH = __uint_as_float(wh & 0xF000u);
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const float4 xl = *reinterpret_cast<const float4*>(xs + m * 256 + 64 * c + 4 * u);
-                            const float4 xh =
-                                *reinterpret_cast<const float4*>(xs + m * 256 + 64 * c + 32 + 4 * u);
-                            slo[m] = fmaf(qA, xl.x, slo[m]);
-                            slo2[m] = fmaf(qC, xl.y, slo2[m]);
-                            slo[m] = fmaf(qE, xl.z, slo[m]);
-                            slo2[m] = fmaf(qG, xl.w, slo2[m]);
-                            shi[m] = fmaf(qB, xh.x, shi[m]);
-                            shi2[m] = fmaf(qD, xh.y, shi2[m]);
-                            shi[m] = fmaf(qF, xh.z, shi[m]);
-                            shi2[m] = fmaf(qH, xh.w, shi2[m]);
-                        }
-                    }
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const float* xsm = xsum + m * 8;
-                        float a = acc[m];
-                        a = fmaf(d1[2 * c], slo[m] + slo2[m], a);
-                        a = fmaf(-mm[2 * c], xsm[2 * c], a);
-                        a = fmaf(d1[2 * c + 1], shi[m] + shi2[m], a);
-                        a = fmaf(-mm[2 * c + 1], xsm[2 * c + 1], a);
-                        acc[m] = a;
-                    }
-                }
-#pragma unroll
-                for (int m = 0; m < MT; ++m) y[m] += (acc[m] * inv_a[m]) * inv_b[m];
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) red[(warp * MT + m) * 32 + lane] = y[m];
-    }
-    __syncthreads();
-
-    // fixed-order reduction over the consumer warps
-    for (int idx = threadIdx.x; idx < MT * 32; idx += kGemvThreads) {
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < kGemvConsumers; ++w) s += red[w * MT * 32 + idx];
-        part[idx] = s;
-    }
-    if (gridDim.y == 1) {
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < MT * 32; idx += kGemvThreads) {
-            const int m = idx >> 5, r = row0 + (idx & 31);
-            if (m < M && r < N) Y[static_cast<int64_t>(m) * N + r] = part[idx];
+            mbar_arrive(bar_full + 8 * s);
         }
     } else {
-        // cluster along y: rank 0 sums the partials of all ranks in rank order
-        cluster_sync_all();
-        if (cluster_ctarank() == 0) {
-            const uint32_t paddr = smem_u32(part);
-            for (int idx = threadIdx.x; idx < MT * 32; idx += kGemvThreads) {
-                const int m = idx >> 5, r = row0 + (idx & 31);
-                float s = 0.f;
-                for (uint32_t rk = 0; rk < gridDim.y; ++rk)
-                    s += ld_shared_cluster_f32(map_shared_rank(paddr + 4 * idx, rk));
-                if (m < M && r < N) Y[static_cast<int64_t>(m) * N + r] = s;
+        // ------------------------------------------------------- consumers ---
+        pdl_wait();  // before any global write
+        const int g = warp / kGemvGroupWarps;                     // group: stages st % G == g
+        const int r = 32 * (warp % kGemvGroupWarps) + lane;       // row within the tile
+        float* grp = reinterpret_cast<float*>(smem + Cfg::kOffGrp);
+        float y[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) y[m] = 0.f;
+        bool ok = true;  // after a timed-out wait the warp only keeps the barrier schedule
+        for (int i = 0; i < nt_local; ++i) {
+            for (int bl = 0; bl < nb; ++bl) {
+                const int st = i * nb + bl;
+                if (st % Cfg::kGroups != g) continue;
+                const int s = st % S;
+                ok = ok && mbar_wait(bar_full + 8 * s, (st / S) & 1, err);
+                if (ok) {
+                    float acc[MT];
+                    block_dot<MT>(smem + Cfg::kOffW + s * kGemvStageBytes + r * kBlockBytes,
+                                  xs_ring + s * MT * 256, xsum_ring + s * MT * 8, acc);
+                    const float* inv = inv_ring + s * MT * 2;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             }
+            // tile done: group 1 hands its sums to group 0 (double-buffered by tile parity)
+            float* gbuf = grp + (i & 1) * MT * kGemvTileRows;
+            if constexpr (Cfg::kGroups == 2) {
+                if (g == 1) {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        gbuf[m * kGemvTileRows + r] = y[m];
+                        y[m] = 0.f;
+                    }
+                }
+                named_bar_sync(1, 32 * Cfg::kConsumers);
+            }
+            if (g == 0) {
+                const int row = (cid + i * ncl) * kGemvTileRows + r;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float v = Cfg::kGroups == 2 ? y[m] + gbuf[m * kGemvTileRows + r] : y[m];
+                    if (C == 1) {
+                        if (m < M && row < N) Y[static_cast<int64_t>(m) * N + row] = v;
+                    } else {
+                        part[m * kGemvTileRows + r] = v;
+                    }
+                    y[m] = 0.f;
+                }
+            }
+        }
+    }
+
+    if (C > 1) {
+        // reduce the C K-slices of this cluster's tile, in rank order
+        cluster_sync_all();
+        const uint32_t paddr = smem_u32(part);
+        for (int e = rank + C * static_cast<int>(threadIdx.x); e < MT * kGemvTileRows;
+             e += C * Cfg::kThreads) {
+            const int m = e / kGemvTileRows;
+            const int row = cid * kGemvTileRows + (e % kGemvTileRows);
+            float sum = 0.f;
+            for (int q = 0; q < C; ++q) sum += ld_shared_cluster_f32(map_shared_rank(paddr + 4 * e, q));
+            if (m < M && row < N) Y[static_cast<int64_t>(m) * N + row] = sum;
         }
         cluster_sync_all();
     }
@@ -294,60 +408,91 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
 
 // ------------------------------------------------------------------ host ---
 
+namespace {
+int g_occ[2][5];  // resident CTAs per SM for each (XB, MT) instantiation
+}
+
 template <int MT, bool XB>
-static cudaError_t set_attr() {
-    return cudaFuncSetAttribute(gemv_kernel<MT, XB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                GemvCfg<MT>::kSmem);
+static cudaError_t set_attr(int slot) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT, XB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<MT>::kSmem);
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<MT, XB>, GemvCfg<MT>::kThreads,
+                                                      GemvCfg<MT>::kSmem);
+    g_occ[XB ? 1 : 0][slot] = occ < 1 ? 1 : occ;
+    return e;
 }
 
 cudaError_t gemv_setup() {
     cudaError_t e = cudaSuccess;
     cudaError_t r;
-#define Q4K_SET(MT)                                          \
-    if ((r = set_attr<MT, false>()) != cudaSuccess) e = r;   \
-    if ((r = set_attr<MT, true>()) != cudaSuccess) e = r;
-    Q4K_SET(1) Q4K_SET(2) Q4K_SET(4) Q4K_SET(8) Q4K_SET(16)
+#define Q4K_SET(MT, SLOT)                                           \
+    if ((r = set_attr<MT, false>(SLOT)) != cudaSuccess) e = r;      \
+    if ((r = set_attr<MT, true>(SLOT)) != cudaSuccess) e = r;
+    Q4K_SET(1, 0) Q4K_SET(2, 1) Q4K_SET(4, 2) Q4K_SET(8, 3) Q4K_SET(16, 4)
 #undef Q4K_SET
     return e;
 }
 
 template <int MT, bool XB>
 static cudaError_t launch_mt(const CUtensorMap& tmapW, const void* X, int M, int N, int K, float* Y,
-                             cudaStream_t stream, const DeviceInfo& dev) {
+                             cudaStream_t stream, const DeviceInfo& dev, int slot, int pdl) {
     const int KB = K / kBlockWeights;
-    const int rg = (N + kGemvRows - 1) / kGemvRows;
-    const int target = 2 * dev.num_sms;
-    int ks = (target + rg - 1) / rg;
-    ks = ks < 1 ? 1 : ks;
-    ks = ks > 8 ? 8 : ks;
-    ks = ks > KB ? KB : ks;
-    const int kb_per = (KB + ks - 1) / ks;
-    ks = (KB + kb_per - 1) / kb_per;
-
+    const int tiles = (N + kGemvTileRows - 1) / kGemvTileRows;
+    const int slots = dev.num_sms * g_occ[XB ? 1 : 0][slot];
+    int C = 1, kb_per = KB, grid;
+    if (tiles >= slots) {
+        // persistent: every CTA streams the same number of tiles (+-1)
+        const int waves = (tiles + slots - 1) / slots;
+        grid = (tiles + waves - 1) / waves;
+    } else {
+        // split K across a cluster, keeping at least 4 super-blocks per CTA
+        C = slots / tiles;
+        const int cmax = KB / 4 < 1 ? 1 : KB / 4;
+        C = C < 1 ? 1 : (C > 8 ? 8 : C);
+        C = C > cmax ? cmax : C;
+        kb_per = (KB + C - 1) / C;
+        C = (KB + kb_per - 1) / kb_per;
+        grid = tiles * C;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rg, ks, 1);
-    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(GemvCfg<MT>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = GemvCfg<MT>::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = ks;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (C > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = C;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, XB>, tmapW, X, M, N, K, Y, kb_per, dev.err);
+    cfg.numAttrs = na;
+    // pdl_flags bit 0: the producer also waits for the preceding grid before
+    // streaming W (cleared only when the caller allows weight prefetch).
+    const int pdl_flags = (pdl == 2) ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, XB>, tmapW, X, M, N, K, Y, tiles, C, kb_per,
+                              pdl_flags, dev.err);
 }
 
 cudaError_t launch_gemv(const CUtensorMap& tmapW, const void* X, bool x_bf16, int M, int N, int K,
-                        float* Y, cudaStream_t stream, const DeviceInfo& dev) {
+                        float* Y, cudaStream_t stream, const DeviceInfo& dev, int pdl) {
     const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
-#define Q4K_CASE(MT)                                                                     \
-    case MT:                                                                             \
-        return x_bf16 ? launch_mt<MT, true>(tmapW, X, M, N, K, Y, stream, dev)           \
-                      : launch_mt<MT, false>(tmapW, X, M, N, K, Y, stream, dev);
+#define Q4K_CASE(MT, SLOT)                                                                  \
+    case MT:                                                                                \
+        return x_bf16 ? launch_mt<MT, true>(tmapW, X, M, N, K, Y, stream, dev, SLOT, pdl)   \
+                      : launch_mt<MT, false>(tmapW, X, M, N, K, Y, stream, dev, SLOT, pdl);
     switch (mt) {
-        Q4K_CASE(1) Q4K_CASE(2) Q4K_CASE(4) Q4K_CASE(8) Q4K_CASE(16)
+        Q4K_CASE(1, 0) Q4K_CASE(2, 1) Q4K_CASE(4, 2) Q4K_CASE(8, 3) Q4K_CASE(16, 4)
     }
 #undef Q4K_CASE
     return cudaErrorInvalidValue;

@@ -17,10 +17,14 @@ struct DeviceInfo {
 cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, cudaStream_t stream,
                            int num_sms);
 
+// Programmatic-dependent-launch mode of a call (see q4k_set_pdl in q4k.h):
+// 0 = plain launch, 1 = overlap the launch with the preceding kernel,
+// 2 = also stream W before the preceding kernel has finished.
+//
 // Split-K GEMV for 1 <= M <= 16 rows of activations (fp32 or bf16 bit patterns).
-// tmapW: 2-D uint8 map {K/256*144, N}, box {144, 32}.
+// tmapW: 2-D uint8 map {K/256*144, N}, box {144, 128}.
 cudaError_t launch_gemv(const CUtensorMap& tmapW, const void* X, bool x_bf16, int M, int N, int K,
-                        float* Y, cudaStream_t stream, const DeviceInfo& dev);
+                        float* Y, cudaStream_t stream, const DeviceInfo& dev, int pdl);
 cudaError_t gemv_setup();
 
 // tcgen05 GEMM for M >= 17 rows of bf16 activations.
@@ -28,7 +32,7 @@ cudaError_t gemv_setup();
 // {K, M}, box {64, BN}, 128-byte swizzle.
 int gemm_pick_bn(int M);
 cudaError_t launch_gemm(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                        float* Y, int BN, cudaStream_t stream, const DeviceInfo& dev);
+                        float* Y, int BN, cudaStream_t stream, const DeviceInfo& dev, int pdl);
 cudaError_t gemm_setup();
 
 }  // namespace q4k

@@ -98,6 +98,22 @@ int q4k_matmul_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16,
                     float* Y, void* stream);
 
 /*
+ * Programmatic dependent launch for every later call in the process (a
+ * decode step issues one call per weight matrix, so the gaps between
+ * back-to-back kernels matter). Returns the previous mode, or
+ * Q4K_ERR_BAD_DIM for an unknown mode.
+ *   0  plain launches (default).
+ *   1  each call's kernel may be scheduled while the preceding kernel on the
+ *      stream is still running; it reads and writes no global memory until
+ *      that kernel has completed. Always safe.
+ *   2  as 1, and the kernel may also start reading its packed weights W
+ *      before the preceding kernel has completed. Only valid when W is not
+ *      written by the kernel that immediately precedes the call on the stream
+ *      (true for model weights).
+ */
+int q4k_set_pdl(int mode);
+
+/*
  * Reads the device error word of the current device (synchronous: waits for
  * all prior work on the device). Returns Q4K_OK or Q4K_ERR_TIMEOUT; with
  * clear != 0 the word is reset. Not capturable.

@@ -87,3 +87,16 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(m, "LIB_PATH", "/nonexistent/libq4k.so")
     with pytest.raises(m.Q4KError):
         m.lib()
+
+
+def test_set_pdl_modes(q4k):
+    L = q4k.lib()
+    old = L.q4k_set_pdl(0)
+    try:
+        assert L.q4k_set_pdl(2) == 0
+        assert L.q4k_set_pdl(1) == 2
+        assert L.q4k_set_pdl(3) == q4k.Q4K_ERR_BAD_DIM
+        assert L.q4k_set_pdl(-1) == q4k.Q4K_ERR_BAD_DIM
+        assert L.q4k_set_pdl(0) == 1
+    finally:
+        L.q4k_set_pdl(old)

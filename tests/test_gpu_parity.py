@@ -99,7 +99,7 @@ def test_dequant_golden_blocks(q4k, oracle_mod):
 @pytest.mark.parametrize("wl", [1, 2, 3, 4])
 def test_dequant_layer0_full_size(q4k, oracle_mod, wl):
     w = synth.WORKLOADS[wl]
-    shapes = {(n, k): m for (_, m, n, k) in w.matrices() if _ == 0 or m == "lm_head"}
+    shapes = {(n, k): m for (layer, m, n, k) in w.matrices() if layer == 0 or m == "lm_head"}
     for (N, K), name in shapes.items():
         Wh = synth.weight_rows(synth.weight_seed(wl, 0, name), N, K)
         _dequant_check(q4k, oracle_mod, Wh, N, K)
@@ -270,3 +270,42 @@ def test_repeat_calls_are_deterministic(q4k):
         b = q4k.matmul(Wd, N, K, X)
         torch.cuda.synchronize()
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_pdl_dependent_chain(q4k, mode):
+    """With programmatic dependent launch, a call whose activations are the
+    previous call's output must still see that output (eager and in a graph)."""
+    K = 2048
+    Ws = [synth.weight_rows(20 + i, K, K).to(DEV) for i in range(4)]
+    Wp = synth.weight_rows(30, 512, K).to(DEV)
+    x0 = synth.activations(31, 1, K).to(DEV)
+
+    def chain():
+        x = x0
+        for W in Ws:  # M=1 GEMV chain: each output is directly the next input
+            x = q4k.matmul(W, K, K, x)
+        xb = x.expand(40, K).to(torch.bfloat16).contiguous()
+        return x, q4k.matmul(Wp, 512, K, xb)  # tcgen05 GEMM after the GEMV chain
+
+    old = q4k.q4k_set_pdl(0)
+    try:
+        ref_x, ref_y = chain()
+        torch.cuda.synchronize()
+        q4k.q4k_set_pdl(mode)
+        for _ in range(3):
+            x, y = chain()
+            torch.cuda.synchronize()
+            assert torch.equal(x, ref_x) and torch.equal(y, ref_y)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            chain()  # warm the allocator on this stream
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                gx, gy = chain()
+            g.replay()
+            s.synchronize()
+        assert torch.equal(gx, ref_x) and torch.equal(gy, ref_y)
+    finally:
+        q4k.q4k_set_pdl(old)
