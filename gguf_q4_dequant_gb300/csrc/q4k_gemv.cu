@@ -12,11 +12,12 @@
 //               than CTA slots, the K range is split across a thread-block
 //               cluster (one K-slice per CTA) and the partial sums are reduced
 //               once, in rank order, through distributed shared memory.
-//   CTA       = 8 consumer warps in two groups of 4 (warp w of a group owns
-//               rows 32w..32w+31 of the tile, one lane per row; the groups take
-//               alternate stages and add their sums once per tile), 1 TMA
-//               producer warp, 1 activation warp. CTAs are persistent over
-//               tiles, so the stage ring streams continuously.
+//   CTA       = consumer warps in G groups of 4 (warp w of a group owns rows
+//               32w..32w+31 of the tile, one lane per row); every group works
+//               on every stage, group g taking chunks [4g/G, 4(g+1)/G) of each
+//               row's super-block, and the groups add their sums once per
+//               tile. Plus 1 TMA producer warp and 1 activation warp. CTAs are
+//               persistent over tiles, so the stage ring streams continuously.
 //
 // Per-weight arithmetic (the unpack happens in registers):
 //   A 4-bit quant q left in place inside its 32-bit word at bit 4p (p = 0..4)
@@ -43,8 +44,8 @@ constexpr int kGemvStageBytes = kGemvTileRows * kBlockBytes;  // 18432
 
 template <int MT>
 struct GemvCfg {
-    // two consumer groups (alternate stages) for small M; one group for
-    // M >= 8, whose register footprint leaves no room for a second
+    // two consumer groups (each half of every super-block) for small M; one
+    // group for M >= 8, whose register footprint leaves no room for a second
     static constexpr int kGroups = MT >= 8 ? 1 : 2;
     static constexpr int kConsumers = kGroups * kGemvGroupWarps;
     static constexpr int kProducerWarp = kConsumers;
@@ -53,9 +54,6 @@ struct GemvCfg {
     // registers: two resident CTAs per SM for small M (measured: more registers
     // per thread buy more overlap than a third CTA would); M >= 8 needs ~250
     static constexpr int kMinBlocks = MT >= 8 ? 1 : 2;
-    // Even, so that slot s is only ever used by consumer group s % 2 (a group
-    // takes the stages of its parity); a group therefore never waits on a
-    // slot more than one phase ahead of it.
     static constexpr int kStages = 4;
     static constexpr int kOffW = 0;
     static constexpr int kOffX = kOffW + kStages * kGemvStageBytes;     // x' [stage][m][256]
@@ -158,7 +156,8 @@ struct XPrefetch {
 };
 // One consumer lane: the contribution of one super-block of its row, scaled by
 // 2^E (acc[m] for each activation row m).
-template <int MT>
+// Chunks C0 .. C0+NC-1 (sub-blocks 2*C0 .. 2*(C0+NC)-1) of the super-block.
+template <int MT, int C0, int NC>
 __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, const float* xsum,
                                           float (&acc)[MT]) {
     const uint4 h = *reinterpret_cast<const uint4*>(P);
@@ -167,18 +166,18 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
     uint64_t dsc[8];  // (d*sc_j, d*sc_j) pairs
     float mm[8];      // dmin*m_j
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float a = d * byte_to_float(sb.sc_lo, j), b = d * byte_to_float(sb.sc_hi, j);
+    for (int j = 2 * C0; j < 2 * (C0 + NC); ++j) {
+        const uint32_t scw = j < 4 ? sb.sc_lo : sb.sc_hi;
+        const uint32_t mw = j < 4 ? sb.m_lo : sb.m_hi;
+        const float a = d * byte_to_float(scw, j & 3);
         dsc[j] = pack2(a, a);
-        dsc[j + 4] = pack2(b, b);
-        mm[j] = dmin * byte_to_float(sb.m_lo, j);
-        mm[j + 4] = dmin * byte_to_float(sb.m_hi, j);
+        mm[j] = dmin * byte_to_float(mw, j & 3);
     }
     uint64_t tot[MT];  // sum over sub-blocks of d*sc_j*S_j, as a pair
 #pragma unroll
     for (int m = 0; m < MT; ++m) tot[m] = 0ull;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = C0; c < C0 + NC; ++c) {
         // the 32 qs bytes of chunk c as four word pairs (u, u+1)
         const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c);
         const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(P + 32 + 32 * c);
@@ -223,7 +222,7 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
         const float* xsm = xsum + m * 8;
         float mins = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mins = fmaf(mm[j], xsm[j], mins);
+        for (int j = 2 * C0; j < 2 * (C0 + NC); ++j) mins = fmaf(mm[j], xsm[j], mins);
         const float2 t = unpack2(tot[m]);
         acc[m] = (t.x + t.y) - mins;
     }
@@ -239,7 +238,6 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 unsigned int* err) {
     using Cfg = GemvCfg<MT>;
     constexpr int S = Cfg::kStages;
-    static_assert(S % Cfg::kGroups == 0, "slot s must belong to consumer group s % G");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const uint32_t sbase = smem_u32(smem);
@@ -263,7 +261,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1 + 32);  // producer (with bytes) + 32 activation lanes
-            mbar_init(bar_empty + 8 * s, kGemvGroupWarps);  // one group consumes a stage
+            mbar_init(bar_empty + 8 * s, Cfg::kConsumers);  // every consumer warp reads every stage
         }
         fence_barrier_init();
     }
@@ -338,7 +336,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     } else {
         // ------------------------------------------------------- consumers ---
         pdl_wait();  // before any global write
-        const int g = warp / kGemvGroupWarps;                     // group: stages st % G == g
+        const int g = warp / kGemvGroupWarps;                     // group: chunk range of every stage
         const int r = 32 * (warp % kGemvGroupWarps) + lane;       // row within the tile
         float* grp = reinterpret_cast<float*>(smem + Cfg::kOffGrp);
         float y[MT];
@@ -348,13 +346,19 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
         for (int i = 0; i < nt_local; ++i) {
             for (int bl = 0; bl < nb; ++bl) {
                 const int st = i * nb + bl;
-                if (st % Cfg::kGroups != g) continue;
                 const int s = st % S;
                 ok = ok && mbar_wait(bar_full + 8 * s, (st / S) & 1, err);
                 if (ok) {
                     float acc[MT];
-                    block_dot<MT>(smem + Cfg::kOffW + s * kGemvStageBytes + r * kBlockBytes,
-                                  xs_ring + s * MT * 256, xsum_ring + s * MT * 8, acc);
+                    const uint8_t* P = smem + Cfg::kOffW + s * kGemvStageBytes + r * kBlockBytes;
+                    const float* xs = xs_ring + s * MT * 256;
+                    const float* xsm = xsum_ring + s * MT * 8;
+                    if constexpr (Cfg::kGroups == 1) {
+                        block_dot<MT, 0, 4>(P, xs, xsm, acc);
+                    } else {
+                        if (g == 0) block_dot<MT, 0, 2>(P, xs, xsm, acc);
+                        else block_dot<MT, 2, 2>(P, xs, xsm, acc);
+                    }
                     const float* inv = inv_ring + s * MT * 2;
 #pragma unroll
                     for (int m = 0; m < MT; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
@@ -447,11 +451,10 @@ static cudaError_t launch_mt(const CUtensorMap& tmapW, const void* X, int M, int
         const int waves = (tiles + slots - 1) / slots;
         grid = (tiles + waves - 1) / waves;
     } else {
-        // split K across a cluster, keeping at least 4 super-blocks per CTA
+        // split K across a cluster (at most 8 CTAs, at least one super-block each)
         C = slots / tiles;
-        const int cmax = KB / 4 < 1 ? 1 : KB / 4;
         C = C < 1 ? 1 : (C > 8 ? 8 : C);
-        C = C > cmax ? cmax : C;
+        C = C > KB ? KB : C;
         kb_per = (KB + C - 1) / C;
         C = (KB + kb_per - 1) / kb_per;
         grid = tiles * C;
