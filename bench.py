@@ -202,12 +202,52 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ GPU arm ---
 
-def _weights(wl, dev, layers):
+def _weights(wl, dev, layers, with_names=False):
     from gguf_q4_dequant_gb300 import synth
     w = synth.WORKLOADS[wl]
+    sel = [(layer, name, N, K) for (layer, name, N, K) in w.matrices() if not layers or layer < layers]
     mats = [(synth.weight_rows(synth.weight_seed(wl, layer, name), N, K, device=dev), N, K)
-            for (layer, name, N, K) in w.matrices() if not layers or layer < layers]
+            for (layer, name, N, K) in sel]
+    if with_names:
+        return w, mats, [(layer, name) for (layer, name, _, _) in sel]
     return w, mats
+
+
+# Matrices of a layer that take the same input: one grouped call each.
+SHARED_INPUT = (("q_proj", "k_proj", "v_proj"), ("gate_proj", "up_proj"))
+
+
+def _grouped_calls(q4k, mats, names, x_dev, y, stream_ptr):
+    """Decode sweep (M = 1) with q/k/v and gate/up as grouped calls; every
+    matrix writes its own slice of `y`."""
+    import ctypes
+    lib = q4k.lib()
+    offs, o = [], 0
+    for (_, N, _) in mats:
+        offs.append(o)
+        o += N
+    groups, i = [], 0
+    while i < len(mats):
+        layer, name = names[i]
+        span = 1
+        for g in SHARED_INPUT:
+            if name == g[0] and [n for (_, n) in names[i:i + len(g)]] == list(g):
+                span = len(g)
+        groups.append(list(range(i, i + span)))
+        i += span
+    calls = []
+    for grp in groups:
+        K = mats[grp[0]][2]
+        Ws = (ctypes.c_void_p * len(grp))(*[mats[j][0].data_ptr() for j in grp])
+        Ns = (ctypes.c_int64 * len(grp))(*[mats[j][1] for j in grp])
+        Ys = (ctypes.c_void_p * len(grp))(*[y.data_ptr() + 4 * offs[j] for j in grp])
+
+        def call(Ws=Ws, Ns=Ns, Ys=Ys, K=K, n=len(grp)):
+            rc = lib.q4k_matmul_multi(n, Ws, Ns, K, x_dev[K].data_ptr(), 1, Ys, stream_ptr)
+            if rc != 0:
+                raise q4k.Q4KError(rc, "grouped sweep")
+        calls.append(call)
+    return calls
 
 
 def _sweep_calls(q4k, mats, x_dev, y, M, bf16, stream_ptr):
@@ -326,14 +366,20 @@ def run_gpu(args):
     times = {}
 
     if args.only in ("all", "decode"):
-        w1, mats1 = _weights(DECODE_WL, dev, args.layers)
+        w1, mats1, names1 = _weights(DECODE_WL, dev, args.layers, with_names=True)
         Ks = sorted({K for (_, _, K) in mats1})
         x_host = {K: synth.activations(synth.x_seed(DECODE_WL, K, 1), 1, K).pin_memory() for K in Ks}
         x_dev = {K: x_host[K].to(dev) for K in Ks}
         y1 = torch.empty(sum(N for (_, N, _) in mats1), device=dev)
-        calls1 = _sweep_calls(q4k, mats1, x_dev, y1, 1, False, sp)
+        calls1 = _grouped_calls(q4k, mats1, names1, x_dev, y1, sp)
         g1 = _capture(torch, calls1, stream)
         bytes1 = sum(Wd.numel() for (Wd, _, _) in mats1)
+        # the same sweep with one call per matrix
+        calls1u = _sweep_calls(q4k, mats1, x_dev, y1, 1, False, sp)
+        g1u = _capture(torch, calls1u, stream)
+        times["decode_per_matrix"] = _time_graph(torch, g1u, stream, args.steps, args.warmup, barrier)
+        launches += args.steps * len(calls1u)
+        del g1u
         # steady load for ~1.5 s so that the clock samples see the working clock
         with torch.cuda.stream(stream):
             t_end = time.time() + 1.5
@@ -342,7 +388,7 @@ def run_gpu(args):
                     g1.replay()
                 torch.cuda.synchronize()
         times["decode"] = _time_graph(torch, g1, stream, args.steps, args.warmup, barrier)
-        launches += args.steps * len(mats1)
+        launches += args.steps * len(calls1)
         # e2e through the public API with host buffers: copy the activation rows
         # in from pinned memory, run the captured q4k_matmul calls, read every
         # output row back.
@@ -364,16 +410,17 @@ def run_gpu(args):
                 e2e_step()
             times["e2e"] = (time.perf_counter() - t0) * 1e3 / args.steps
             barrier()
-        launches += args.steps * len(mats1)
-        bpl = bytes1 / len(mats1)
-        gemv_ms = times["decode"] / len(mats1)  # in-graph, gaps between launches included
+        launches += args.steps * len(calls1)
+        bpl = bytes1 / len(calls1)
+        gemv_ms = times["decode"] / len(calls1)  # in-graph, gaps between launches included
         achieved = bpl / (gemv_ms * 1e-3) / 1e9
         out.update({
             "unit": "GB/s",
             "config": {"workload": f"{w1.name}: {len(mats1)} Q4_K matrices, "
                                    f"{bytes1 / 1e6:.1f} MB packed, M=1 fp32 activations",
                        "l2": "inputs larger than L2 (every step streams all weights from HBM)",
-                       "launch": f"one CUDA graph per sweep, q4k_set_pdl({args.pdl})",
+                       "launch": f"one CUDA graph per sweep, q4k_set_pdl({args.pdl}); q/k/v and "
+                                 f"gate/up as grouped calls ({len(calls1)} launches per step)",
                        "parallelism": f"replicas x{ws}"},
             "roofline": {"bound": "hbm", "kernel": "gemv_kernel<1,f32>", "achieved": round(achieved, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
@@ -386,6 +433,7 @@ def run_gpu(args):
         })
         del g1
         out["_bytes1"] = bytes1
+        out["_names1"] = names1
         for (Wd, _, _) in mats1:
             del Wd
         del mats1, calls1
@@ -428,6 +476,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     times = dict(zip(keys, t.tolist()))
+    out.pop("_names1", None) if "decode" not in times else None
     out["device_error"] = q4k.q4k_device_error()
     out["gpu_launches"] = launches
     if rank != 0:
@@ -436,6 +485,10 @@ def run_gpu(args):
         b1 = out.pop("_bytes1")
         out["value"] = round(ws * b1 / (times["decode"] * 1e-3) / 1e9, 2)
         out["ms_per_step"] = round(times["decode"], 5)
+        out["decode_one_call_per_matrix"] = {
+            "value": round(ws * b1 / (times["decode_per_matrix"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(times["decode_per_matrix"], 5),
+            "launches_per_step": len(out.pop("_names1"))}
         out["e2e"]["value"] = round(ws * b1 / (times["e2e"] * 1e-3) / 1e9, 2)
         out["e2e"]["ms_per_step"] = round(times["e2e"], 4)
     if "prefill" in times:

@@ -25,7 +25,8 @@ Q4K_ERR_TIMEOUT = -6
 
 #: every symbol include/q4k.h declares
 EXPORTS = ("q4k_status_string", "q4k_init", "q4k_dequant", "q4k_matmul", "q4k_matmul_bf16",
-           "q4k_set_pdl", "q4k_device_error")
+           "q4k_matmul_multi", "q4k_matmul_multi_bf16", "q4k_set_pdl", "q4k_device_error")
+MAX_GROUP = 8
 
 
 _STATUS_NAMES = {Q4K_OK: "Q4K_OK", Q4K_ERR_NULL: "Q4K_ERR_NULL", Q4K_ERR_BAD_DIM: "Q4K_ERR_BAD_DIM",
@@ -63,6 +64,12 @@ def lib() -> ctypes.CDLL:
             L.q4k_matmul.restype = ctypes.c_int
             L.q4k_matmul_bf16.argtypes = [vp, i64, i64, vp, i64, vp, vp]
             L.q4k_matmul_bf16.restype = ctypes.c_int
+            vpp = ctypes.POINTER(ctypes.c_void_p)
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            L.q4k_matmul_multi.argtypes = [ctypes.c_int, vpp, i64p, i64, vp, i64, vpp, vp]
+            L.q4k_matmul_multi.restype = ctypes.c_int
+            L.q4k_matmul_multi_bf16.argtypes = [ctypes.c_int, vpp, i64p, i64, vp, i64, vpp, vp]
+            L.q4k_matmul_multi_bf16.restype = ctypes.c_int
             L.q4k_set_pdl.argtypes = [ctypes.c_int]
             L.q4k_set_pdl.restype = ctypes.c_int
             L.q4k_device_error.argtypes = [ctypes.c_int]
@@ -135,6 +142,25 @@ def q4k_matmul_bf16(W, N: int, K: int, X, M: int, Y, stream=None):
     _check_dtype(Y, torch.float32, "Y")
     _check(lib().q4k_matmul_bf16(_ptr(W), N, K, _ptr(X), M, _ptr(Y), _stream(stream)),
            "q4k_matmul_bf16")
+
+
+def q4k_matmul_multi(Ws, Ns, K: int, X, M: int, Ys, stream=None):
+    """Y_i[M, N_i] = X[M, K] * W_i^T for matrices sharing K and X (fp32 or bf16 X)."""
+    import torch
+    count = len(Ws)
+    if not (len(Ns) == len(Ys) == count):
+        raise ValueError("Ws, Ns and Ys must have the same length")
+    for W, Y in zip(Ws, Ys):
+        _check_dtype(W, torch.uint8, "W")
+        _check_dtype(Y, torch.float32, "Y")
+    bf16 = not isinstance(X, int) and X.dtype == torch.bfloat16
+    if not bf16:
+        _check_dtype(X, torch.float32, "X")
+    w_arr = (ctypes.c_void_p * count)(*[_ptr(W) for W in Ws])
+    n_arr = (ctypes.c_int64 * count)(*[int(n) for n in Ns])
+    y_arr = (ctypes.c_void_p * count)(*[_ptr(Y) for Y in Ys])
+    fn = lib().q4k_matmul_multi_bf16 if bf16 else lib().q4k_matmul_multi
+    _check(fn(count, w_arr, n_arr, K, _ptr(X), M, y_arr, _stream(stream)), "q4k_matmul_multi")
 
 
 def q4k_set_pdl(mode: int) -> int:

@@ -8,6 +8,9 @@
 //                   M >  16  -> K2 over consecutive 16-row slices of X
 //   q4k_matmul_bf16 M <= 16  -> K2 gemv_kernel (bf16 activations)
 //                   M >= 17  -> K3 gemm_kernel (tcgen05, TMEM accumulators)
+//   q4k_matmul_multi[_bf16]  -> the same, for up to 8 matrices sharing K and X:
+//                   one K2 launch for all of them (M <= 16), one K3 launch each
+//                   (M >= 17)
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -122,19 +125,57 @@ int encode_x_bf16(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN)
     return r == CUDA_SUCCESS ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
-int run_gemv(const void* W, int64_t N, int64_t K, const void* X, bool xb, int64_t M, float* Y,
-             cudaStream_t stream, const DeviceInfo& dev) {
-    CUtensorMap tw;
-    int rc = encode_w(&tw, W, N, K, 128);
-    if (rc != Q4K_OK) return rc;
+// One GEMV launch per 16-row slice of X over `count` matrices sharing K and X.
+int run_gemv(int count, const void* const* W, const int64_t* N, int64_t K, const void* X, bool xb,
+             int64_t M, float* const* Y, cudaStream_t stream, const DeviceInfo& dev) {
+    GemvGroup grp;
+    grp.count = count;
+    grp.tile_start[0] = 0;
+    for (int i = 0; i < count; ++i) {
+        const int rc = encode_w(&grp.maps[i], W[i], N[i], K, 128);
+        if (rc != Q4K_OK) return rc;
+        grp.N[i] = static_cast<int>(N[i]);
+        grp.tile_start[i + 1] = grp.tile_start[i] + static_cast<int>((N[i] + 127) / 128);
+    }
     const size_t xelem = xb ? 2 : 4;
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mc = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
         const void* Xc = static_cast<const uint8_t*>(X) + static_cast<size_t>(m0) * K * xelem;
-        if (launch_gemv(tw, Xc, xb, mc, static_cast<int>(N), static_cast<int>(K), Y + m0 * N, stream,
-                        dev, g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
+        for (int i = 0; i < count; ++i) grp.Y[i] = Y[i] + m0 * N[i];
+        if (launch_gemv(grp, Xc, xb, mc, static_cast<int>(K), stream, dev,
+                        g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
             return Q4K_ERR_CUDA;
     }
+    return Q4K_OK;
+}
+
+int run_gemm(const void* W, int64_t N, int64_t K, const uint16_t* X, int64_t M, float* Y,
+             cudaStream_t stream, const DeviceInfo& dev) {
+    const int BN = gemm_pick_bn(static_cast<int>(M));
+    CUtensorMap tw, tx;
+    int rc;
+    if ((rc = encode_w(&tw, W, N, K, 128)) != Q4K_OK) return rc;
+    if ((rc = encode_x_bf16(&tx, X, M, K, BN)) != Q4K_OK) return rc;
+    if (launch_gemm(tw, tx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), Y, BN,
+                    stream, dev, g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
+        return Q4K_ERR_CUDA;
+    return Q4K_OK;
+}
+
+// Checks shared by the single and grouped matmul calls.
+int check_matmul(int count, const void* const* W, const int64_t* N, int64_t K, const void* X,
+                 int64_t M, float* const* Y) {
+    if (!W || !N || !X || !Y) return Q4K_ERR_NULL;
+    if (count < 1 || count > kMaxGroup) return Q4K_ERR_BAD_DIM;
+    if (M < 1 || M > (int64_t(1) << 31) - 1) return Q4K_ERR_BAD_DIM;
+    for (int i = 0; i < count; ++i) {
+        if (!W[i] || !Y[i]) return Q4K_ERR_NULL;
+        const int rc = check_dims(N[i], K);
+        if (rc != Q4K_OK) return rc;
+    }
+    if (!aligned16(X)) return Q4K_ERR_ALIGN;
+    for (int i = 0; i < count; ++i)
+        if (!aligned16(W[i]) || !aligned16(Y[i])) return Q4K_ERR_ALIGN;
     return Q4K_OK;
 }
 
@@ -179,33 +220,44 @@ int q4k_dequant(const void* W, int64_t N, int64_t K, float* out_f32, void* strea
 int q4k_matmul(const void* W, int64_t N, int64_t K, const float* X, int64_t M, float* Y,
                void* stream) {
     if (!W || !X || !Y) return Q4K_ERR_NULL;
-    int rc = check_dims(N, K);
+    int rc = check_matmul(1, &W, &N, K, X, M, &Y);
     if (rc != Q4K_OK) return rc;
-    if (M < 1 || M > (int64_t(1) << 31) - 1) return Q4K_ERR_BAD_DIM;
-    if (!aligned16(W) || !aligned16(X) || !aligned16(Y)) return Q4K_ERR_ALIGN;
     const DeviceInfo* dev = nullptr;
     if ((rc = current_device(&dev)) != Q4K_OK) return rc;
-    return run_gemv(W, N, K, X, false, M, Y, static_cast<cudaStream_t>(stream), *dev);
+    return run_gemv(1, &W, &N, K, X, false, M, &Y, static_cast<cudaStream_t>(stream), *dev);
 }
 
 int q4k_matmul_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16, int64_t M,
                     float* Y, void* stream) {
     if (!W || !X_bf16 || !Y) return Q4K_ERR_NULL;
-    int rc = check_dims(N, K);
+    int rc = check_matmul(1, &W, &N, K, X_bf16, M, &Y);
     if (rc != Q4K_OK) return rc;
-    if (M < 1 || M > (int64_t(1) << 31) - 1) return Q4K_ERR_BAD_DIM;
-    if (!aligned16(W) || !aligned16(X_bf16) || !aligned16(Y)) return Q4K_ERR_ALIGN;
     const DeviceInfo* dev = nullptr;
     if ((rc = current_device(&dev)) != Q4K_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M <= 16) return run_gemv(W, N, K, X_bf16, true, M, Y, st, *dev);
-    const int BN = gemm_pick_bn(static_cast<int>(M));
-    CUtensorMap tw, tx;
-    if ((rc = encode_w(&tw, W, N, K, 128)) != Q4K_OK) return rc;
-    if ((rc = encode_x_bf16(&tx, X_bf16, M, K, BN)) != Q4K_OK) return rc;
-    if (launch_gemm(tw, tx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), Y, BN, st,
-                    *dev, g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
-        return Q4K_ERR_CUDA;
+    if (M <= 16) return run_gemv(1, &W, &N, K, X_bf16, true, M, &Y, st, *dev);
+    return run_gemm(W, N, K, X_bf16, M, Y, st, *dev);
+}
+
+int q4k_matmul_multi(int count, const void* const* W, const int64_t* N, int64_t K, const float* X,
+                     int64_t M, float* const* Y, void* stream) {
+    int rc = check_matmul(count, W, N, K, X, M, Y);
+    if (rc != Q4K_OK) return rc;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = current_device(&dev)) != Q4K_OK) return rc;
+    return run_gemv(count, W, N, K, X, false, M, Y, static_cast<cudaStream_t>(stream), *dev);
+}
+
+int q4k_matmul_multi_bf16(int count, const void* const* W, const int64_t* N, int64_t K,
+                          const uint16_t* X_bf16, int64_t M, float* const* Y, void* stream) {
+    int rc = check_matmul(count, W, N, K, X_bf16, M, Y);
+    if (rc != Q4K_OK) return rc;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = current_device(&dev)) != Q4K_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M <= 16) return run_gemv(count, W, N, K, X_bf16, true, M, Y, st, *dev);
+    for (int i = 0; i < count; ++i)
+        if ((rc = run_gemm(W[i], N[i], K, X_bf16, M, Y[i], st, *dev)) != Q4K_OK) return rc;
     return Q4K_OK;
 }
 

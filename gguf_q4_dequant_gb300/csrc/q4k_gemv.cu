@@ -10,8 +10,12 @@
 //               memory as [row][144] (a stage, 18 KB).
 //   K-slice   = a contiguous range of super-blocks. When there are fewer tiles
 //               than CTA slots, the K range is split across a thread-block
-//               cluster (one K-slice per CTA) and the partial sums are reduced
-//               once, in rank order, through distributed shared memory.
+//               cluster (one K-slice per CTA); ranks 1..C-1 store their partial
+//               sums into rank 0's shared memory and arrive on its mbarrier, and
+//               rank 0 adds them in rank order (deterministic).
+//   group     = up to 8 weight matrices that share K and the activations (q, k
+//               and v of a layer; gate and up) are one launch: their tiles are
+//               numbered consecutively and each has its own TMA map and output.
 //   CTA       = consumer warps in G groups of 4 (warp w of a group owns rows
 //               32w..32w+31 of the tile, one lane per row); every group works
 //               on every stage, group g taking chunks [4g/G, 4(g+1)/G) of each
@@ -59,10 +63,10 @@ struct GemvCfg {
     static constexpr int kOffX = kOffW + kStages * kGemvStageBytes;     // x' [stage][m][256]
     static constexpr int kOffXs = kOffX + kStages * MT * 256 * 4;        // sums [stage][m][8]
     static constexpr int kOffInv = kOffXs + kStages * MT * 8 * 4;        // 2^-E [stage][m][2]
-    static constexpr int kOffPart = kOffInv + kStages * MT * 2 * 4;      // cluster partials [m][128]
-    static constexpr int kOffGrp = kOffPart + MT * kGemvTileRows * 4;    // group-1 sums [2][m][128]
-    static constexpr int kOffBar = kOffGrp + 2 * MT * kGemvTileRows * 4; // full[S], empty[S]
-    static constexpr int kSmem = kOffBar + 2 * kStages * 8 + 128;        // + alignment slack
+    static constexpr int kOffRed = kOffInv + kStages * MT * 2 * 4;       // ranks 1..7: [7][m][128]
+    static constexpr int kOffGrp = kOffRed + 7 * MT * kGemvTileRows * 4; // group-1 sums [2][m][128]
+    static constexpr int kOffBar = kOffGrp + 2 * MT * kGemvTileRows * 4; // full[S], empty[S], red
+    static constexpr int kSmem = kOffBar + (2 * kStages + 1) * 8 + 128;  // + alignment slack
 };
 
 // Loads 8 consecutive activations of row m as fp32 (zeros past M).
@@ -231,11 +235,17 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
 // Grid: gridDim.x = (number of clusters) * C; a cluster of C CTAs along x
 // shares tiles and splits K into C slices of kb_per super-blocks. With C > 1
 // every cluster owns exactly one tile.
+// Matrix of the group that owns global tile t.
+__device__ __forceinline__ int group_matrix(const GemvGroup& g, int t) {
+    int i = 0;
+    while (i + 1 < g.count && t >= g.tile_start[i + 1]) ++i;
+    return i;
+}
+
 template <int MT, bool XB>
 __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks)
-    gemv_kernel(const __grid_constant__ CUtensorMap tmapW, const void* __restrict__ X, int M, int N,
-                int K, float* __restrict__ Y, int tiles, int C, int kb_per, int pdl_flags,
-                unsigned int* err) {
+    gemv_kernel(const __grid_constant__ GemvGroup grp, const void* __restrict__ X, int M, int K,
+                int C, int kb_per, int pdl_flags, unsigned int* err) {
     using Cfg = GemvCfg<MT>;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -248,6 +258,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     const int ncl = gridDim.x / C;
     const int kb0 = rank * kb_per;
     const int nb = min(KB, kb0 + kb_per) - kb0;
+    const int tiles = grp.tile_start[grp.count];
     const int nt_local = (tiles - cid + ncl - 1) / ncl;  // tiles cid, cid + ncl, ...
     const int total = nt_local * nb;                     // stages this CTA streams
 
@@ -256,32 +267,38 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     float* xs_ring = reinterpret_cast<float*>(smem + Cfg::kOffX);
     float* xsum_ring = reinterpret_cast<float*>(smem + Cfg::kOffXs);
     float* inv_ring = reinterpret_cast<float*>(smem + Cfg::kOffInv);
-    float* part = reinterpret_cast<float*>(smem + Cfg::kOffPart);
+    float* red = reinterpret_cast<float*>(smem + Cfg::kOffRed);
+    const uint32_t bar_red = bar_empty + 8 * S;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1 + 32);  // producer (with bytes) + 32 activation lanes
             mbar_init(bar_empty + 8 * s, Cfg::kConsumers);  // every consumer warp reads every stage
         }
+        // rank 0 of a cluster: the other ranks' group-0 consumer threads
+        mbar_init(bar_red, C > 1 ? (C - 1) * 32 * kGemvGroupWarps : 1);
         fence_barrier_init();
     }
     __syncthreads();
+    if (C > 1) cluster_arrive_relaxed();  // the barriers above are ready for remote arrivals
     if (threadIdx.x == 0) pdl_launch_dependents();
 
     if (warp == Cfg::kProducerWarp) {
         // ---------------------------------------------------- TMA producer ---
         if (lane == 0) {
-            tma_prefetch_desc(&tmapW);
+            for (int i = 0; i < grp.count; ++i) tma_prefetch_desc(&grp.maps[i]);
             if (pdl_flags & 1) pdl_wait();
             const uint64_t pol = policy_evict_first();
             for (int st = 0; st < total; ++st) {
                 const int s = st % S;
                 if (!mbar_wait(bar_empty + 8 * s, ((st / S) & 1) ^ 1, err)) break;
                 const int t = cid + (st / nb) * ncl;
+                const int mi = group_matrix(grp, t);
                 const int b = kb0 + st % nb;
                 mbar_arrive_expect_tx(bar_full + 8 * s, kGemvStageBytes);
-                tma_load_2d_hint(sbase + Cfg::kOffW + s * kGemvStageBytes, &tmapW, b * kBlockBytes,
-                                 t * kGemvTileRows, bar_full + 8 * s, pol);
+                tma_load_2d_hint(sbase + Cfg::kOffW + s * kGemvStageBytes, &grp.maps[mi],
+                                 b * kBlockBytes, (t - grp.tile_start[mi]) * kGemvTileRows,
+                                 bar_full + 8 * s, pol);
             }
             // the CTA must not exit while a copy into its shared memory is in flight
             for (int st = total - S < 0 ? 0 : total - S; st < total; ++st)
@@ -338,7 +355,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
         pdl_wait();  // before any global write
         const int g = warp / kGemvGroupWarps;                     // group: chunk range of every stage
         const int r = 32 * (warp % kGemvGroupWarps) + lane;       // row within the tile
-        float* grp = reinterpret_cast<float*>(smem + Cfg::kOffGrp);
+        float* gsum = reinterpret_cast<float*>(smem + Cfg::kOffGrp);
         float y[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) y[m] = 0.f;
@@ -367,7 +384,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             }
             // tile done: group 1 hands its sums to group 0 (double-buffered by tile parity)
-            float* gbuf = grp + (i & 1) * MT * kGemvTileRows;
+            float* gbuf = gsum + (i & 1) * MT * kGemvTileRows;
             if constexpr (Cfg::kGroups == 2) {
                 if (g == 1) {
 #pragma unroll
@@ -379,35 +396,49 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 named_bar_sync(1, 32 * Cfg::kConsumers);
             }
             if (g == 0) {
-                const int row = (cid + i * ncl) * kGemvTileRows + r;
+                if constexpr (Cfg::kGroups == 2) {
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const float v = Cfg::kGroups == 2 ? y[m] + gbuf[m * kGemvTileRows + r] : y[m];
-                    if (C == 1) {
-                        if (m < M && row < N) Y[static_cast<int64_t>(m) * N + row] = v;
-                    } else {
-                        part[m * kGemvTileRows + r] = v;
+                    for (int m = 0; m < MT; ++m) y[m] += gbuf[m * kGemvTileRows + r];
+                }
+                if (C == 1) {  // C > 1: one tile per CTA, reduced across the cluster below
+                    const int t = cid + i * ncl;
+                    const int mi = group_matrix(grp, t);
+                    const int row = (t - grp.tile_start[mi]) * kGemvTileRows + r;
+                    const int Nm = grp.N[mi];
+                    float* Ym = grp.Y[mi];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (m < M && row < Nm) Ym[static_cast<int64_t>(m) * Nm + row] = y[m];
+                        y[m] = 0.f;
                     }
-                    y[m] = 0.f;
                 }
             }
         }
-    }
-
-    if (C > 1) {
-        // reduce the C K-slices of this cluster's tile, in rank order
-        cluster_sync_all();
-        const uint32_t paddr = smem_u32(part);
-        for (int e = rank + C * static_cast<int>(threadIdx.x); e < MT * kGemvTileRows;
-             e += C * Cfg::kThreads) {
-            const int m = e / kGemvTileRows;
-            const int row = cid * kGemvTileRows + (e % kGemvTileRows);
-            float sum = 0.f;
-            for (int q = 0; q < C; ++q) sum += ld_shared_cluster_f32(map_shared_rank(paddr + 4 * e, q));
-            if (m < M && row < N) Y[static_cast<int64_t>(m) * N + row] = sum;
+        if (C > 1 && g == 0) {
+            // K-slices of this cluster's tile: ranks 1.. push into rank 0, which adds in rank order
+            cluster_wait();
+            if (rank != 0) {
+                const uint32_t dst = map_shared_rank(smem_u32(red + (rank - 1) * MT * kGemvTileRows), 0);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) st_shared_cluster_f32(dst + 4 * (m * kGemvTileRows + r), y[m]);
+                mbar_arrive_remote(map_shared_rank(bar_red, 0));
+            } else if (mbar_wait(bar_red, 0, err)) {
+                const int mi = group_matrix(grp, cid);
+                const int row = (cid - grp.tile_start[mi]) * kGemvTileRows + r;
+                const int Nm = grp.N[mi];
+                float* Ym = grp.Y[mi];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    float v = y[m];
+                    for (int q = 1; q < C; ++q) v += red[(q - 1) * MT * kGemvTileRows + m * kGemvTileRows + r];
+                    if (m < M && row < Nm) Ym[static_cast<int64_t>(m) * Nm + row] = v;
+                }
+            }
+            return;
         }
-        cluster_sync_all();
     }
+    if (C > 1) cluster_wait();  // every thread that arrived also waits
+
 }
 
 // ------------------------------------------------------------------ host ---
@@ -440,10 +471,10 @@ cudaError_t gemv_setup() {
 }
 
 template <int MT, bool XB>
-static cudaError_t launch_mt(const CUtensorMap& tmapW, const void* X, int M, int N, int K, float* Y,
-                             cudaStream_t stream, const DeviceInfo& dev, int slot, int pdl) {
+static cudaError_t launch_mt(const GemvGroup& grp, const void* X, int M, int K, cudaStream_t stream,
+                             const DeviceInfo& dev, int slot, int pdl) {
     const int KB = K / kBlockWeights;
-    const int tiles = (N + kGemvTileRows - 1) / kGemvTileRows;
+    const int tiles = grp.tile_start[grp.count];
     const int slots = dev.num_sms * g_occ[XB ? 1 : 0][slot];
     int C = 1, kb_per = KB, grid;
     if (tiles >= slots) {
@@ -483,17 +514,16 @@ static cudaError_t launch_mt(const CUtensorMap& tmapW, const void* X, int M, int
     // pdl_flags bit 0: the producer also waits for the preceding grid before
     // streaming W (cleared only when the caller allows weight prefetch).
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, XB>, tmapW, X, M, N, K, Y, tiles, C, kb_per,
-                              pdl_flags, dev.err);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, XB>, grp, X, M, K, C, kb_per, pdl_flags, dev.err);
 }
 
-cudaError_t launch_gemv(const CUtensorMap& tmapW, const void* X, bool x_bf16, int M, int N, int K,
-                        float* Y, cudaStream_t stream, const DeviceInfo& dev, int pdl) {
+cudaError_t launch_gemv(const GemvGroup& grp, const void* X, bool x_bf16, int M, int K,
+                        cudaStream_t stream, const DeviceInfo& dev, int pdl) {
     const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
-#define Q4K_CASE(MT, SLOT)                                                                  \
-    case MT:                                                                                \
-        return x_bf16 ? launch_mt<MT, true>(tmapW, X, M, N, K, Y, stream, dev, SLOT, pdl)   \
-                      : launch_mt<MT, false>(tmapW, X, M, N, K, Y, stream, dev, SLOT, pdl);
+#define Q4K_CASE(MT, SLOT)                                                            \
+    case MT:                                                                          \
+        return x_bf16 ? launch_mt<MT, true>(grp, X, M, K, stream, dev, SLOT, pdl)     \
+                      : launch_mt<MT, false>(grp, X, M, K, stream, dev, SLOT, pdl);
     switch (mt) {
         Q4K_CASE(1, 0) Q4K_CASE(2, 1) Q4K_CASE(4, 2) Q4K_CASE(8, 3) Q4K_CASE(16, 4)
     }

@@ -21,10 +21,18 @@ cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, c
 // 0 = plain launch, 1 = overlap the launch with the preceding kernel,
 // 2 = also stream W before the preceding kernel has finished.
 //
-// Split-K GEMV for 1 <= M <= 16 rows of activations (fp32 or bf16 bit patterns).
-// tmapW: 2-D uint8 map {K/256*144, N}, box {144, 128}.
-cudaError_t launch_gemv(const CUtensorMap& tmapW, const void* X, bool x_bf16, int M, int N, int K,
-                        float* Y, cudaStream_t stream, const DeviceInfo& dev, int pdl);
+// Split-K GEMV for 1 <= M <= 16 rows of activations (fp32 or bf16 bit patterns)
+// over up to kMaxGroup weight matrices that share K and X (one launch).
+constexpr int kMaxGroup = 8;
+struct alignas(64) GemvGroup {
+    CUtensorMap maps[kMaxGroup];     // W_i: 2-D uint8 map {K/256*144, N_i}, box {144, 128}
+    float* Y[kMaxGroup];             // Y_i: fp32 [M][N_i]
+    int N[kMaxGroup];
+    int tile_start[kMaxGroup + 1];   // prefix sums of ceil(N_i / 128)
+    int count;
+};
+cudaError_t launch_gemv(const GemvGroup& grp, const void* X, bool x_bf16, int M, int K,
+                        cudaStream_t stream, const DeviceInfo& dev, int pdl);
 cudaError_t gemv_setup();
 
 // tcgen05 GEMM for M >= 17 rows of bf16 activations.

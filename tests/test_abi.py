@@ -100,3 +100,21 @@ def test_set_pdl_modes(q4k):
         assert L.q4k_set_pdl(0) == 1
     finally:
         L.q4k_set_pdl(old)
+
+
+def test_grouped_call_host_checks(q4k):
+    import ctypes as C
+    L = q4k.lib()
+    W = (C.c_void_p * 3)(A16, A16, A16)
+    Y = (C.c_void_p * 3)(A16, A16, A16)
+    N = (C.c_int64 * 3)(256, 128, 7)
+    assert L.q4k_matmul_multi(0, W, N, 256, A16, 1, Y, None) == q4k.Q4K_ERR_BAD_DIM
+    assert L.q4k_matmul_multi(9, W, N, 256, A16, 1, Y, None) == q4k.Q4K_ERR_BAD_DIM
+    assert L.q4k_matmul_multi(3, None, N, 256, A16, 1, Y, None) == q4k.Q4K_ERR_NULL
+    Wn = (C.c_void_p * 3)(A16, None, A16)
+    assert L.q4k_matmul_multi(3, Wn, N, 256, A16, 1, Y, None) == q4k.Q4K_ERR_NULL
+    Nb = (C.c_int64 * 3)(256, 0, 7)
+    assert L.q4k_matmul_multi_bf16(3, W, Nb, 256, A16, 1, Y, None) == q4k.Q4K_ERR_BAD_DIM
+    Ym = (C.c_void_p * 3)(A16, A16 + 4, A16)
+    assert L.q4k_matmul_multi(3, W, N, 256, A16, 1, Ym, None) == q4k.Q4K_ERR_ALIGN
+    assert L.q4k_matmul_multi(3, W, N, 300, A16, 1, Y, None) == q4k.Q4K_ERR_BAD_DIM

@@ -309,3 +309,56 @@ def test_pdl_dependent_chain(q4k, mode):
         assert torch.equal(gx, ref_x) and torch.equal(gy, ref_y)
     finally:
         q4k.q4k_set_pdl(old)
+
+
+@pytest.mark.parametrize("xdt", ["f32", "bf16"])
+def test_grouped_matmul(q4k, oracle_mod, xdt):
+    """q4k_matmul_multi: several matrices sharing K and X in one call (ragged N,
+    including sizes that split K across a cluster and ones that do not)."""
+    K = 1536
+    Ns = [384, 128, 96, 3000, 1]
+    Whs = [synth.weight_rows(8000 + i, n, K) for i, n in enumerate(Ns)]
+    Wds = [w.to(DEV) for w in Whs]
+    dt = torch.bfloat16 if xdt == "bf16" else torch.float32
+    Ms = (1, 3, 16, 40) if xdt == "bf16" else (1, 3, 16, 20)
+    for M in Ms:
+        X = synth.activations(8100 + M, M, K, dt)
+        Ys = [torch.full((M, n), float("nan"), device=DEV) for n in Ns]
+        q4k.q4k_matmul_multi(Wds, Ns, K, X.to(DEV), M, Ys)
+        torch.cuda.synchronize()
+        tol = TOL_GEMM if (dt == torch.bfloat16 and M > 16) else TOL_GEMV
+        Xo = _x_for_oracle(oracle_mod, X)
+        for Wh, n, Y in zip(Whs, Ns, Ys):
+            Yref, A = oracle_mod.matmul(Wh.numpy(), n, K, Xo)
+            got = Y.cpu().double().numpy()
+            assert np.all(np.isfinite(got))
+            assert float(np.max(np.abs(got - Yref) / (tol * A + 1e-30))) <= 1.0
+
+
+def test_grouped_matmul_in_graph_with_pdl(q4k):
+    K = 2048
+    Ns = [2048, 512, 512]
+    Wds = [synth.weight_rows(8200 + i, n, K).to(DEV) for i, n in enumerate(Ns)]
+    X = synth.activations(8300, 1, K).to(DEV)
+    ref = [q4k.matmul(W, n, K, X) for W, n in zip(Wds, Ns)]
+    torch.cuda.synchronize()
+    old = q4k.q4k_set_pdl(2)
+    try:
+        s = torch.cuda.Stream()
+        Ys = [torch.zeros(1, n, device=DEV) for n in Ns]
+        with torch.cuda.stream(s):
+            q4k.q4k_matmul_multi(Wds, Ns, K, X, 1, Ys)
+            s.synchronize()
+            first = [y.clone() for y in Ys]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                q4k.q4k_matmul_multi(Wds, Ns, K, X, 1, Ys)
+            for y in Ys:
+                y.zero_()
+            g.replay()
+            s.synchronize()
+        for a, b, r in zip(first, Ys, ref):
+            assert torch.equal(a, b)
+            assert torch.allclose(a, r, rtol=0, atol=1e-3)
+    finally:
+        q4k.q4k_set_pdl(old)
