@@ -151,12 +151,13 @@ int run_gemv(int count, const void* const* W, const int64_t* N, int64_t K, const
 
 int run_gemm(const void* W, int64_t N, int64_t K, const uint16_t* X, int64_t M, float* Y,
              cudaStream_t stream, const DeviceInfo& dev) {
-    const int BN = gemm_pick_bn(static_cast<int>(M));
+    const GemmPlan plan =
+        gemm_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev.num_sms);
     CUtensorMap tw, tx;
     int rc;
     if ((rc = encode_w(&tw, W, N, K, 128)) != Q4K_OK) return rc;
-    if ((rc = encode_x_bf16(&tx, X, M, K, BN)) != Q4K_OK) return rc;
-    if (launch_gemm(tw, tx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), Y, BN,
+    if ((rc = encode_x_bf16(&tx, X, M, K, plan.BN)) != Q4K_OK) return rc;
+    if (launch_gemm(tw, tx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), Y, plan,
                     stream, dev, g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
         return Q4K_ERR_CUDA;
     return Q4K_OK;

@@ -11,14 +11,20 @@
 //   accumulator    = 128 TMEM lanes x BN fp32 columns
 // so each dequantised weight tile is reused across all BN tokens of the tile.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer: packed W super-block tiles {144 B, 128 rows}
 //               and X tiles {64 k, BN rows} (128-byte swizzle)
 //   warp 1      TMEM allocator and MMA issuer (one elected thread)
-//   warps 2..5  dequantisers (thread t <-> weight row t of the tile): read the
-//               packed block from shared memory, write 64 bf16 weights per
-//               k-step into the swizzled A tile; then the epilogue (TMEM ->
-//               registers -> Y, 128-byte coalesced stores per token column).
+//   warps 2..17 dequantisers (thread t <-> weight row t % 128; t / 128 picks
+//               the nibble half and which 16 of the chunk's 32 qs bytes): read
+//               the packed block from shared memory and write 16 bf16 weights
+//               per k-step into the swizzled A tile; then the epilogue (TMEM ->
+//               registers -> Y, 128-byte coalesced stores per token column;
+//               four warps per TMEM lane quadrant).
+// When the tiles alone cannot fill the GPU, K is split across a thread-block
+// cluster of C CTAs: each CTA leaves its partial accumulator in its own shared
+// memory, and rank r adds the C partials of rows [r*128/C, (r+1)*128/C) in
+// rank order through distributed shared memory (deterministic).
 // All pipeline waits are bounded (see mbar_wait).
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
@@ -27,54 +33,68 @@ namespace q4k {
 
 constexpr int kGemmBM = 128;
 constexpr int kGemmKStep = 64;                       // bf16 k per A/B stage (one 128-byte row)
-constexpr int kGemmThreads = 192;
-constexpr int kGemmWStages = 2;
+constexpr int kGemmDequantWarps = 16;
+constexpr int kGemmDequantThreads = 32 * kGemmDequantWarps;   // 512
+constexpr int kGemmThreads = 64 + kGemmDequantThreads;        // 576
+constexpr int kGemmWStages = 3;  // a DRAM round trip is longer than one super-block of MMAs
 constexpr int kGemmWStageBytes = kGemmBM * kBlockBytes;   // 18432
 constexpr int kGemmAStageBytes = kGemmBM * 128;           // 16384
 
+// Separate rings for the dequantised A tiles and the TMA-loaded X (B) tiles:
+// B is made as deep as shared memory allows, since its refill is an L2 round
+// trip issued only when the MMA of the slot's previous k-step completes.
 template <int BN>
 struct GemmCfg {
-    static constexpr int kABStages = BN == 256 ? 3 : 4;
+    static constexpr int kAStages = BN == 256 ? 3 : 4;
+    static constexpr int kBStages = BN == 256 ? 3 : BN == 128 ? 5 : BN == 64 ? 6 : 8;
     static constexpr int kBStageBytes = BN * 128;
     static constexpr int kOffA = 0;                                            // 1024-aligned
-    static constexpr int kOffB = kOffA + kABStages * kGemmAStageBytes;         // 1024-aligned
-    static constexpr int kOffW = kOffB + kABStages * kBStageBytes;
+    static constexpr int kOffB = kOffA + kAStages * kGemmAStageBytes;          // 1024-aligned
+    static constexpr int kOffW = kOffB + kBStages * kBStageBytes;
     static constexpr int kOffBar = kOffW + kGemmWStages * kGemmWStageBytes;
-    // barriers: w_full[2], w_empty[2], a_full[S], b_full[S], ab_empty[S], acc_full, tmem slot
-    static constexpr int kNumBars = 2 * kGemmWStages + 3 * kABStages + 1;
+    // barriers: w_full[W], w_empty[W], a_full[SA], a_empty[SA], b_full[SB], b_empty[SB], acc_full
+    static constexpr int kNumBars = 2 * kGemmWStages + 2 * kAStages + 2 * kBStages + 1;
     static constexpr int kOffTmem = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffTmem + 16 + 1024;   // + alignment slack
     static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
 };
 
-// Converts 8 low (or high) nibbles of two qs words into 8 bf16 weights
-// w = d1*q - m1 (fp32 FMA, then round-to-nearest-even to bf16).
-__device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, int shift, float d1, float nm1) {
-    const uint32_t a = (w0 >> shift) & 0x0F0F0F0Fu;
-    const uint32_t b = (w1 >> shift) & 0x0F0F0F0Fu;
-    float f[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        // 0x4B0000qq is 2^23 + q exactly; subtracting 2^23 leaves q
-        f[i] = __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7440u | i)) - 8388608.f;
-        f[4 + i] = __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7440u | i)) - 8388608.f;
-    }
+// Eight weights of one nibble half (hh) from the qs word pair P = (w0, w1)
+// (bytes b0..b7, little-endian): w = d1*q - m1 in fp32, rounded to bf16.
+// A nibble masked in place at bit s of a word, OR'ed with 0x4B000000, is the
+// float 2^23 + 2^s*q exactly (s + 4 <= 23); pairs are handled with 64-bit
+// masks and the paired fp32 ops: bytes (i, i+4) of the pair form one fp32 pair.
+// Bytes 2 and 3 are first brought down by a 64-bit shift by 16. d1s0 / d1s1 are
+// (d1*2^-s, d1*2^-s) for s = 4*hh and 8 + 4*hh; nm1 is (-m1, -m1).
+__device__ __forceinline__ uint4 dequant8x(uint64_t P, int hh, uint64_t d1s0, uint64_t d1s1,
+                                           uint64_t nm1) {
+    const uint64_t magic = 0x4B0000004B000000ull;
+    const uint64_t neg = 0xCB000000CB000000ull;  // (-2^23, -2^23)
+    const uint64_t m0 = 0x0000000F0000000Full << (4 * hh);
+    const uint64_t m1 = 0x00000F0000000F00ull << (4 * hh);
+    const uint64_t S = P >> 16;
+    const uint64_t f0 = fma2(add2((P & m0) | magic, neg), d1s0, nm1);  // (w_b0, w_b4)
+    const uint64_t f1 = fma2(add2((P & m1) | magic, neg), d1s1, nm1);  // (w_b1, w_b5)
+    const uint64_t f2 = fma2(add2((S & m0) | magic, neg), d1s0, nm1);  // (w_b2, w_b6)
+    const uint64_t f3 = fma2(add2((S & m1) | magic, neg), d1s1, nm1);  // (w_b3, w_b7)
+    const float2 a = unpack2(f0), b = unpack2(f1), c = unpack2(f2), d = unpack2(f3);
     uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 p =
-            __floats2bfloat162_rn(fmaf(f[2 * i], d1, nm1), fmaf(f[2 * i + 1], d1, nm1));
-        o[i] = *reinterpret_cast<const uint32_t*>(&p);
-    }
+    __nv_bfloat162 t;
+    t = __floats2bfloat162_rn(a.x, b.x); o[0] = *reinterpret_cast<uint32_t*>(&t);
+    t = __floats2bfloat162_rn(c.x, d.x); o[1] = *reinterpret_cast<uint32_t*>(&t);
+    t = __floats2bfloat162_rn(a.y, b.y); o[2] = *reinterpret_cast<uint32_t*>(&t);
+    t = __floats2bfloat162_rn(c.y, d.y); o[3] = *reinterpret_cast<uint32_t*>(&t);
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ CUtensorMap tmapX,
-                int M, int N, int K, float* __restrict__ Y, int pdl_flags, unsigned int* err) {
+                int M, int N, int K, float* __restrict__ Y, int C, int kb_per, int pdl_flags,
+                unsigned int* err) {
     using Cfg = GemmCfg<BN>;
-    constexpr int S = Cfg::kABStages;
+    constexpr int SA = Cfg::kAStages;
+    constexpr int SB = Cfg::kBStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -84,26 +104,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kGemmBM;
     const int m0 = blockIdx.y * BN;
-    const int KB = K / kBlockWeights;
-    const int nks = K / kGemmKStep;
+    const int rank = blockIdx.z;  // cluster rank along z = K-slice
+    const int kb0 = rank * kb_per;
+    const int KB = min(K / kBlockWeights, kb0 + kb_per) - kb0;  // super-blocks of this K-slice
+    const int nks = 4 * KB;                                       // 64-k steps of this K-slice
+    const int ks0 = 4 * kb0;
 
     const uint32_t bw_full = sbase + Cfg::kOffBar;
     const uint32_t bw_empty = bw_full + 8 * kGemmWStages;
     const uint32_t ba_full = bw_empty + 8 * kGemmWStages;
-    const uint32_t bb_full = ba_full + 8 * S;
-    const uint32_t bab_empty = bb_full + 8 * S;
-    const uint32_t bacc = bab_empty + 8 * S;
+    const uint32_t ba_empty = ba_full + 8 * SA;
+    const uint32_t bb_full = ba_empty + 8 * SA;
+    const uint32_t bb_empty = bb_full + 8 * SB;
+    const uint32_t bacc = bb_empty + 8 * SB;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmem);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kGemmWStages; ++i) {
             mbar_init(bw_full + 8 * i, 1);
-            mbar_init(bw_empty + 8 * i, 128);
+            mbar_init(bw_empty + 8 * i, kGemmDequantThreads);
         }
-        for (int i = 0; i < S; ++i) {
-            mbar_init(ba_full + 8 * i, 128);
+        for (int i = 0; i < SA; ++i) {
+            mbar_init(ba_full + 8 * i, kGemmDequantThreads);
+            mbar_init(ba_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < SB; ++i) {
             mbar_init(bb_full + 8 * i, 1);
-            mbar_init(bab_empty + 8 * i, 1);
+            mbar_init(bb_empty + 8 * i, 1);
         }
         mbar_init(bacc, 1);
         fence_barrier_init();
@@ -137,14 +164,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (!mbar_wait(bw_empty + 8 * ws, ((sb / kGemmWStages) & 1) ^ 1, err)) break;
                     mbar_arrive_expect_tx(bw_full + 8 * ws, kGemmWStageBytes);
                     tma_load_2d_hint(sbase + Cfg::kOffW + ws * kGemmWStageBytes, &tmapW,
-                                     sb * kBlockBytes, n0, bw_full + 8 * ws, pol_w);
+                                     (kb0 + sb) * kBlockBytes, n0, bw_full + 8 * ws, pol_w);
                 }
-                const int s = ks % S;
-                if (!mbar_wait(bab_empty + 8 * s, ((ks / S) & 1) ^ 1, err)) break;
+                const int s = ks % SB;
+                if (!mbar_wait(bb_empty + 8 * s, ((ks / SB) & 1) ^ 1, err)) break;
                 if (ks == 0 && !(pdl_flags & 1)) pdl_wait();
                 mbar_arrive_expect_tx(bb_full + 8 * s, Cfg::kBStageBytes);
-                tma_load_2d_hint(sbase + Cfg::kOffB + s * Cfg::kBStageBytes, &tmapX, ks * kGemmKStep,
-                                 m0, bb_full + 8 * s, pol_x);
+                tma_load_2d_hint(sbase + Cfg::kOffB + s * Cfg::kBStageBytes, &tmapX,
+                                 (ks0 + ks) * kGemmKStep, m0, bb_full + 8 * s, pol_x);
             }
         }
         __syncwarp();
@@ -154,60 +181,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, BN);
             bool ok = true;
             for (int ks = 0; ks < nks && ok; ++ks) {
-                const int s = ks % S;
-                const uint32_t ph = (ks / S) & 1;
-                ok = mbar_wait(ba_full + 8 * s, ph, err) && mbar_wait(bb_full + 8 * s, ph, err);
+                const int sa = ks % SA, sbs = ks % SB;
+                ok = mbar_wait(ba_full + 8 * sa, (ks / SA) & 1, err) &&
+                     mbar_wait(bb_full + 8 * sbs, (ks / SB) & 1, err);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a0 = sbase + Cfg::kOffA + s * kGemmAStageBytes;
-                const uint32_t b0 = sbase + Cfg::kOffB + s * Cfg::kBStageBytes;
+                const uint32_t a0 = sbase + Cfg::kOffA + sa * kGemmAStageBytes;
+                const uint32_t b0 = sbase + Cfg::kOffB + sbs * Cfg::kBStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < kGemmKStep / 16; ++kk)
                     tc_mma_bf16(tmem, sw128_desc(a0 + 32 * kk), sw128_desc(b0 + 32 * kk), idesc,
                                 (ks | kk) != 0);
-                tc_commit(bab_empty + 8 * s);
+                tc_commit(ba_empty + 8 * sa);
+                tc_commit(bb_empty + 8 * sbs);
             }
             tc_commit(bacc);
         }
         __syncwarp();
     } else {
         // ------------------------------------------ dequantisers (A) ---
-        const int t = threadIdx.x - 64;  // weight row within the tile
+        const int t = threadIdx.x - 64;
+        const int r = t & (kGemmBM - 1);  // weight row within the tile
+        const int hh = (t >> 7) & 1;      // 0: low nibbles (sub-block 2c), 1: high (2c+1)
+        const int p = t >> 8;             // which 16 of the chunk's 32 qs bytes
         bool ok = true;
         for (int sb = 0; sb < KB && ok; ++sb) {
             const int ws = sb % kGemmWStages;
             if (!mbar_wait(bw_full + 8 * ws, (sb / kGemmWStages) & 1, err)) { ok = false; break; }
-            const uint8_t* P = smem + Cfg::kOffW + ws * kGemmWStageBytes + t * kBlockBytes;
-            const uint4 h = *reinterpret_cast<const uint4*>(P);
-            const ScaleBytes scb = decode_scales(h.y, h.z, h.w);
-            const float d = half_lo(h.x), dmin = half_hi(h.x);
+            const uint8_t* P = smem + Cfg::kOffW + ws * kGemmWStageBytes + r * kBlockBytes;
+            const uint4 hd = *reinterpret_cast<const uint4*>(P);
+            const ScaleBytes scb = decode_scales(hd.y, hd.z, hd.w);
+            const float d = half_lo(hd.x), dmin = half_hi(hd.x);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int ks = sb * 4 + c;
-                const int s = ks % S;
-                if (!mbar_wait(bab_empty + 8 * s, ((ks / S) & 1) ^ 1, err)) { ok = false; break; }
-                const uint32_t scw = c < 2 ? scb.sc_lo : scb.sc_hi;
-                const uint32_t mw = c < 2 ? scb.m_lo : scb.m_hi;
-                const int jb = (2 * c) & 3;
-                const float d1l = d * static_cast<float>(byte_of(scw, jb));
-                const float m1l = -(dmin * static_cast<float>(byte_of(mw, jb)));
-                const float d1h = d * static_cast<float>(byte_of(scw, jb + 1));
-                const float m1h = -(dmin * static_cast<float>(byte_of(mw, jb + 1)));
-                const uint4 qa = *reinterpret_cast<const uint4*>(P + 16 + 32 * c);
-                const uint4 qb = *reinterpret_cast<const uint4*>(P + 32 + 32 * c);
-                // 16-byte chunk j of the row holds k = 8j .. 8j+7 of this 64-k step:
-                //   j < 4: low nibbles of qs bytes 8j..8j+7 (sub-block 2c)
-                //   j >= 4: high nibbles of qs bytes 8(j-4)..  (sub-block 2c+1)
-                uint8_t* arow = smem + Cfg::kOffA + s * kGemmAStageBytes + t * 128;
-                const int sw = t & 7;
-                const uint32_t wq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    *reinterpret_cast<uint4*>(arow + ((j ^ sw) << 4)) =
-                        dequant8(wq[2 * j], wq[2 * j + 1], 0, d1l, m1l);
-                    *reinterpret_cast<uint4*>(arow + (((j + 4) ^ sw) << 4)) =
-                        dequant8(wq[2 * j], wq[2 * j + 1], 4, d1h, m1h);
-                }
+                const int s = ks % SA;
+                if (!mbar_wait(ba_empty + 8 * s, ((ks / SA) & 1) ^ 1, err)) { ok = false; break; }
+                const int j = 2 * c + hh;  // sub-block
+                const uint32_t scw = j < 4 ? scb.sc_lo : scb.sc_hi;
+                const uint32_t mw = j < 4 ? scb.m_lo : scb.m_hi;
+                const float d1 = d * byte_to_float(scw, j & 3);
+                const float m1 = dmin * byte_to_float(mw, j & 3);
+                const float d1s0 = d1 * exp2i(-4 * hh), d1s1 = d1 * exp2i(-8 - 4 * hh);
+                const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c + 16 * p);
+                // output chunk 4hh + 2p + v holds k = 32hh + 16p + 8v .. +7 of this 64-k step
+                uint8_t* arow = smem + Cfg::kOffA + s * kGemmAStageBytes + r * 128;
+                const int sw = r & 7;
+                const uint64_t D0 = pack2(d1s0, d1s0), D1 = pack2(d1s1, d1s1), NM = pack2(-m1, -m1);
+                *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p) ^ sw) << 4)) =
+                    dequant8x(q.x, hh, D0, D1, NM);
+                *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p + 1) ^ sw) << 4)) =
+                    dequant8x(q.y, hh, D0, D1, NM);
                 fence_proxy_async_smem();
                 mbar_arrive(ba_full + 8 * s);
             }
@@ -215,24 +239,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
 
         // ------------------------------------------------- epilogue ---
-        if (ok && mbar_wait(bacc, 0, err)) {
+        // four warps per TMEM lane quadrant, each taking a quarter of the BN columns
+        const int q = warp & 3;                      // TMEM lane quadrant this warp may access
+        const int half = (warp - 2) >> 2;            // column slice 0..3
+        constexpr int kCols = BN >= 128 ? BN / 4 : 32;
+        const bool active = half * kCols < BN;
+        if (ok && mbar_wait(bacc, 0, err) && active) {
             tc_fence_after();
-            const int q = warp & 3;  // TMEM lane quadrant this warp may access
-            const int n = n0 + 32 * q + lane;
+            const int row = 32 * q + lane;
+            float* part = reinterpret_cast<float*>(smem + Cfg::kOffA);  // [BN][128], C > 1
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
+            for (int cc = half * kCols; cc < (half + 1) * kCols; cc += 32) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * cc, v);
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + cc, v);
                 tmem_ld_wait();
-                if (n < N) {
+                if (C == 1) {
+                    const int n = n0 + row;
+                    if (n < N) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int m = m0 + 32 * cc + j;
-                        if (m < M) Y[static_cast<int64_t>(m) * N + n] = __uint_as_float(v[j]);
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const int m = m0 + cc + jj;
+                            if (m < M) Y[static_cast<int64_t>(m) * N + n] = __uint_as_float(v[jj]);
+                        }
                     }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) part[(cc + jj) * kGemmBM + row] = __uint_as_float(v[jj]);
                 }
             }
         }
+    }
+    if (C > 1) {
+        // every CTA's partial tile is in its shared memory: rank `rank` adds
+        // rows [rank*rows, (rank+1)*rows) of all C partials in rank order
+        cluster_sync_all();
+        const int rows = (kGemmBM + C - 1) / C;
+        const int r0 = rank * rows;
+        const int nr = min(kGemmBM, r0 + rows) - r0;
+        const uint32_t pbase = sbase + Cfg::kOffA;
+        for (int idx = threadIdx.x; idx < nr * BN; idx += kGemmThreads) {
+            const int col = idx / nr;
+            const int row = r0 + idx % nr;
+            const uint32_t off = 4u * static_cast<uint32_t>(col * kGemmBM + row);
+            float acc = 0.f;
+            for (int qr = 0; qr < C; ++qr) acc += ld_shared_cluster_f32(map_shared_rank(pbase + off, qr));
+            const int n = n0 + row, m = m0 + col;
+            if (n < N && m < M) Y[static_cast<int64_t>(m) * N + n] = acc;
+        }
+        cluster_sync_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -244,7 +298,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------------------ host ---
 
-int gemm_pick_bn(int M) { return M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
+// Tile width BN (tokens) and K-split C for an M x N x K product, from a
+// wave-count cost model: a CTA spends max(2*BN, 300) cycles per 64-k step (the
+// MMA of a 128 x BN x 64 step versus the dequantising warps), plus ~2000 cycles
+// of prologue and pipeline fill and its epilogue (~4000 more with a split).
+GemmPlan gemm_plan(int M, int N, int K, int num_sms) {
+    const int KB = K / kBlockWeights;
+    const int ntiles = (N + kGemmBM - 1) / kGemmBM;
+    const int bns[2] = {M <= 32 ? 32 : M <= 64 ? 64 : 128, M > 128 ? 256 : 0};
+    const int cs[6] = {1, 2, 3, 4, 6, 8};
+    GemmPlan best{bns[0], 1, KB};
+    double best_cost = 1e300;
+    for (int bn : bns) {
+        if (bn == 0) continue;
+        const int mtiles = (M + bn - 1) / bn;
+        for (int c : cs) {
+            if (c > KB) break;
+            const int kb_per = (KB + c - 1) / c;
+            const int ce = (KB + kb_per - 1) / kb_per;
+            const long ctas = static_cast<long>(ntiles) * mtiles * ce;
+            const long waves = (ctas + num_sms - 1) / num_sms;
+            const double tk = 2.0 * bn > 300.0 ? 2.0 * bn : 300.0;
+            const double cost = static_cast<double>(waves) *
+                                (4.0 * kb_per * tk + 2000.0 + (ce > 1 ? 4000.0 + 8.0 * bn : 4.0 * bn));
+            if (cost < best_cost * 0.999) {
+                best_cost = cost;
+                best = GemmPlan{bn, ce, kb_per};
+            }
+        }
+    }
+    return best;
+}
 
 template <int BN>
 static cudaError_t set_attr() {
@@ -263,30 +347,42 @@ cudaError_t gemm_setup() {
 
 template <int BN>
 static cudaError_t launch_bn(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                             float* Y, cudaStream_t stream, unsigned int* err, int pdl) {
+                             float* Y, const GemmPlan& plan, cudaStream_t stream, unsigned int* err,
+                             int pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + kGemmBM - 1) / kGemmBM, (M + BN - 1) / BN, 1);
+    cfg.gridDim = dim3((N + kGemmBM - 1) / kGemmBM, (M + BN - 1) / BN, plan.C);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = GemmCfg<BN>::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (plan.C > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = plan.C;
+        ++na;
     }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, tmapW, tmapX, M, N, K, Y, pdl_flags, err);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, tmapW, tmapX, M, N, K, Y, plan.C, plan.kb_per,
+                              pdl_flags, err);
 }
 
 cudaError_t launch_gemm(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                        float* Y, int BN, cudaStream_t stream, const DeviceInfo& dev, int pdl) {
-    switch (BN) {
-        case 32: return launch_bn<32>(tmapW, tmapX, M, N, K, Y, stream, dev.err, pdl);
-        case 64: return launch_bn<64>(tmapW, tmapX, M, N, K, Y, stream, dev.err, pdl);
-        case 128: return launch_bn<128>(tmapW, tmapX, M, N, K, Y, stream, dev.err, pdl);
-        case 256: return launch_bn<256>(tmapW, tmapX, M, N, K, Y, stream, dev.err, pdl);
+                        float* Y, const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev,
+                        int pdl) {
+    switch (plan.BN) {
+        case 32: return launch_bn<32>(tmapW, tmapX, M, N, K, Y, plan, stream, dev.err, pdl);
+        case 64: return launch_bn<64>(tmapW, tmapX, M, N, K, Y, plan, stream, dev.err, pdl);
+        case 128: return launch_bn<128>(tmapW, tmapX, M, N, K, Y, plan, stream, dev.err, pdl);
+        case 256: return launch_bn<256>(tmapW, tmapX, M, N, K, Y, plan, stream, dev.err, pdl);
     }
     return cudaErrorInvalidValue;
 }

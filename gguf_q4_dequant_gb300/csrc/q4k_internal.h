@@ -38,9 +38,15 @@ cudaError_t gemv_setup();
 // tcgen05 GEMM for M >= 17 rows of bf16 activations.
 // tmapW: 2-D uint8 map {K/256*144, N}, box {144, 128}; tmapX: 2-D bf16 map
 // {K, M}, box {64, BN}, 128-byte swizzle.
-int gemm_pick_bn(int M);
+struct GemmPlan {
+    int BN;      // tokens per tile (MMA N)
+    int C;       // K-split factor (cluster size along z)
+    int kb_per;  // super-blocks per K-slice
+};
+GemmPlan gemm_plan(int M, int N, int K, int num_sms);
 cudaError_t launch_gemm(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                        float* Y, int BN, cudaStream_t stream, const DeviceInfo& dev, int pdl);
+                        float* Y, const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev,
+                        int pdl);
 cudaError_t gemm_setup();
 
 }  // namespace q4k
