@@ -13,7 +13,8 @@
 //
 // Warp roles (320 threads):
 //   warp 0      TMA producer: packed W super-block tiles {144 B, 128 rows}
-//               and X tiles {64 k, BN rows} (128-byte swizzle)
+//               and X tiles {64 k, BN rows} (128-byte swizzle), two rings
+//               refilled independently
 //   warp 1      TMEM allocator and MMA issuer (one elected thread)
 //   warps 2..17 dequantisers (thread t <-> weight row t % 128; t / 128 picks
 //               the nibble half and which 16 of the chunk's 32 qs bytes): read
@@ -157,46 +158,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             if (pdl_flags & 1) pdl_wait();
-            for (int ks = 0; ks < nks; ++ks) {
-                if ((ks & 3) == 0) {
-                    const int sb = ks >> 2;
+            // The W ring (refilled when the dequantisers release a stage) and
+            // the X ring (refilled when the MMA of a stage completes) advance
+            // independently: the thread polls both and never blocks on one
+            // while the other could be refilled. Bounded like mbar_wait.
+            bool x_ready = (pdl_flags & 1) != 0;  // preceding grid already complete
+            int sb = 0, ks = 0;
+            uint32_t idle = 0;
+            unsigned long long t0 = 0;
+            while (sb < KB || ks < nks) {
+                bool progress = false;
+                if (sb < KB) {
                     const int ws = sb % kGemmWStages;
-                    if (!mbar_wait(bw_empty + 8 * ws, ((sb / kGemmWStages) & 1) ^ 1, err)) break;
-                    mbar_arrive_expect_tx(bw_full + 8 * ws, kGemmWStageBytes);
-                    tma_load_2d_hint(sbase + Cfg::kOffW + ws * kGemmWStageBytes, &tmapW,
-                                     (kb0 + sb) * kBlockBytes, n0, bw_full + 8 * ws, pol_w);
+                    if (mbar_test_wait(bw_empty + 8 * ws, ((sb / kGemmWStages) & 1) ^ 1)) {
+                        mbar_arrive_expect_tx(bw_full + 8 * ws, kGemmWStageBytes);
+                        tma_load_2d_hint(sbase + Cfg::kOffW + ws * kGemmWStageBytes, &tmapW,
+                                         (kb0 + sb) * kBlockBytes, n0, bw_full + 8 * ws, pol_w);
+                        ++sb;
+                        progress = true;
+                    }
                 }
-                const int s = ks % SB;
-                if (!mbar_wait(bb_empty + 8 * s, ((ks / SB) & 1) ^ 1, err)) break;
-                if (ks == 0 && !(pdl_flags & 1)) pdl_wait();
-                mbar_arrive_expect_tx(bb_full + 8 * s, Cfg::kBStageBytes);
-                tma_load_2d_hint(sbase + Cfg::kOffB + s * Cfg::kBStageBytes, &tmapX,
-                                 (ks0 + ks) * kGemmKStep, m0, bb_full + 8 * s, pol_x);
+                if (ks < nks) {
+                    const int s = ks % SB;
+                    if (mbar_test_wait(bb_empty + 8 * s, ((ks / SB) & 1) ^ 1)) {
+                        if (!x_ready) {
+                            pdl_wait();
+                            x_ready = true;
+                        }
+                        mbar_arrive_expect_tx(bb_full + 8 * s, Cfg::kBStageBytes);
+                        tma_load_2d_hint(sbase + Cfg::kOffB + s * Cfg::kBStageBytes, &tmapX,
+                                         (ks0 + ks) * kGemmKStep, m0, bb_full + 8 * s, pol_x);
+                        ++ks;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle = 0;
+                } else if (idle++ == 0) {
+                    t0 = globaltimer();
+                } else if ((idle & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+                    atomicOr(err, 1u);
+                    break;
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer ---
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, BN);
-            bool ok = true;
-            for (int ks = 0; ks < nks && ok; ++ks) {
-                const int sa = ks % SA, sbs = ks % SB;
-                ok = mbar_wait(ba_full + 8 * sa, (ks / SA) & 1, err) &&
-                     mbar_wait(bb_full + 8 * sbs, (ks / SB) & 1, err);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t a0 = sbase + Cfg::kOffA + sa * kGemmAStageBytes;
-                const uint32_t b0 = sbase + Cfg::kOffB + sbs * Cfg::kBStageBytes;
+        // The whole warp runs the loop and the waits (so stage indices and
+        // descriptors stay warp-uniform); one elected lane issues.
+        constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, BN);
+        for (int ks = 0; ks < nks; ++ks) {
+            const int sa = ks % SA, sbs = ks % SB;
+            bool ok = mbar_wait(ba_full + 8 * sa, (ks / SA) & 1, err) &&
+                      mbar_wait(bb_full + 8 * sbs, (ks / SB) & 1, err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            if (elect_one()) {
+                const uint64_t a0 = sw128_desc(sbase + Cfg::kOffA + sa * kGemmAStageBytes);
+                const uint64_t b0 = sw128_desc(sbase + Cfg::kOffB + sbs * Cfg::kBStageBytes);
 #pragma unroll
-                for (int kk = 0; kk < kGemmKStep / 16; ++kk)
-                    tc_mma_bf16(tmem, sw128_desc(a0 + 32 * kk), sw128_desc(b0 + 32 * kk), idesc,
-                                (ks | kk) != 0);
+                for (int kk = 0; kk < kGemmKStep / 16; ++kk)  // +32 bytes per k16 = +2 in the address field
+                    tc_mma_bf16(tmem, a0 + 2 * kk, b0 + 2 * kk, idesc, (ks | kk) != 0);
                 tc_commit(ba_empty + 8 * sa);
                 tc_commit(bb_empty + 8 * sbs);
             }
-            tc_commit(bacc);
+            __syncwarp();
         }
+        if (elect_one()) tc_commit(bacc);
         __syncwarp();
     } else {
         // ------------------------------------------ dequantisers (A) ---
