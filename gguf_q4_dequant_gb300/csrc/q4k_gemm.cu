@@ -23,9 +23,10 @@
 //               registers -> Y, 128-byte coalesced stores per token column;
 //               four warps per TMEM lane quadrant).
 // When the tiles alone cannot fill the GPU, K is split across a thread-block
-// cluster of C CTAs: each CTA leaves its partial accumulator in its own shared
-// memory, and rank r adds the C partials of rows [r*128/C, (r+1)*128/C) in
-// rank order through distributed shared memory (deterministic).
+// cluster of C CTAs: each CTA pushes the accumulator rows owned by rank r
+// (rows [r*ceil(128/C), ...)) from TMEM into rank r's shared memory through
+// distributed shared memory, and rank r adds the C partials in rank order
+// (deterministic).
 // All pipeline waits are bounded (see mbar_wait).
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
@@ -58,6 +59,8 @@ struct GemmCfg {
     static constexpr int kOffTmem = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffTmem + 16 + 1024;   // + alignment slack
     static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+    // split-K slots: C <= 8 slots of BN x ceil(128 / C) floats in the A/B region
+    static_assert((kGemmBM + 8) * BN * 4 <= kOffW, "split-K slots must fit in the A/B region");
 };
 
 // Eight weights of one nibble half (hh) from the qs word pair P = (w0, w1)
@@ -145,6 +148,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (threadIdx.x == 0) pdl_launch_dependents();
+    // epilogue assignment of the dequantising warps (set in their branch)
+    bool acc_ok = false;
+    int epi_cols = 0, epi_c0 = 0, epi_row = 0;
     // Every warp except the producer waits for the preceding grid here; the
     // producer waits before its first activation load (and, unless weight
     // prefetch is allowed, before its first weight load).
@@ -271,19 +277,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // four warps per TMEM lane quadrant, each taking a quarter of the BN columns
         const int q = warp & 3;                      // TMEM lane quadrant this warp may access
         const int half = (warp - 2) >> 2;            // column slice 0..3
-        constexpr int kCols = BN >= 128 ? BN / 4 : 32;
-        const bool active = half * kCols < BN;
-        if (ok && mbar_wait(bacc, 0, err) && active) {
+        epi_cols = BN >= 128 ? BN / 4 : 32;
+        epi_c0 = half * epi_cols;
+        epi_row = 32 * q + lane;
+        acc_ok = ok && mbar_wait(bacc, 0, err) && epi_c0 < BN;
+        if (acc_ok) {
             tc_fence_after();
-            const int row = 32 * q + lane;
-            float* part = reinterpret_cast<float*>(smem + Cfg::kOffA);  // [BN][128], C > 1
+            if (C == 1) {
+                const int n = n0 + epi_row;
 #pragma unroll 1
-            for (int cc = half * kCols; cc < (half + 1) * kCols; cc += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + cc, v);
-                tmem_ld_wait();
-                if (C == 1) {
-                    const int n = n0 + row;
+                for (int cc = epi_c0; cc < epi_c0 + epi_cols; cc += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + cc, v);
+                    tmem_ld_wait();
                     if (n < N) {
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) {
@@ -291,31 +297,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             if (m < M) Y[static_cast<int64_t>(m) * N + n] = __uint_as_float(v[jj]);
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) part[(cc + jj) * kGemmBM + row] = __uint_as_float(v[jj]);
                 }
             }
         }
     }
     if (C > 1) {
-        // every CTA's partial tile is in its shared memory: rank `rank` adds
-        // rows [rank*rows, (rank+1)*rows) of all C partials in rank order
-        cluster_sync_all();
+        // Split K: rank r owns rows [r*rows, r*rows + nr) of the tile. Once
+        // every CTA's MMAs are complete (first cluster barrier) the A/B region
+        // of every CTA is free, and each CTA pushes the rows it does not own
+        // straight from TMEM into the owner's region (posted remote stores:
+        // slot [source rank][column][owned row]); after the second barrier
+        // each owner adds the C slots in rank order (deterministic).
         const int rows = (kGemmBM + C - 1) / C;
-        const int r0 = rank * rows;
-        const int nr = min(kGemmBM, r0 + rows) - r0;
+        const uint32_t slot_bytes = 4u * static_cast<uint32_t>(BN * rows);
         const uint32_t pbase = sbase + Cfg::kOffA;
-        for (int idx = threadIdx.x; idx < nr * BN; idx += kGemmThreads) {
-            const int col = idx / nr;
-            const int row = r0 + idx % nr;
-            const uint32_t off = 4u * static_cast<uint32_t>(col * kGemmBM + row);
-            float acc = 0.f;
-            for (int qr = 0; qr < C; ++qr) acc += ld_shared_cluster_f32(map_shared_rank(pbase + off, qr));
-            const int n = n0 + row, m = m0 + col;
-            if (n < N && m < M) Y[static_cast<int64_t>(m) * N + n] = acc;
+        cluster_sync_all();
+        if (acc_ok) {
+            tc_fence_after();
+            const int owner = epi_row / rows;
+            const uint32_t dst = map_shared_rank(pbase, owner) + rank * slot_bytes +
+                                 4u * static_cast<uint32_t>(epi_row - owner * rows);
+#pragma unroll 1
+            for (int cc = epi_c0; cc < epi_c0 + epi_cols; cc += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(epi_row & ~31) << 16) + cc, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    st_shared_cluster_f32(dst + 4u * static_cast<uint32_t>((cc + jj) * rows),
+                                          __uint_as_float(v[jj]));
+            }
         }
         cluster_sync_all();
+        const int r0 = rank * rows;
+        const int nr = min(kGemmBM, r0 + rows) - r0;
+        const float* part = reinterpret_cast<const float*>(smem + Cfg::kOffA);
+        for (int idx = threadIdx.x; idx < nr * BN; idx += kGemmThreads) {
+            const int col = idx / nr;
+            const int rl = idx - col * nr;
+            float acc = 0.f;
+            for (int src = 0; src < C; ++src) acc += part[src * (BN * rows) + col * rows + rl];
+            const int n = n0 + r0 + rl, m = m0 + col;
+            if (n < N && m < M) Y[static_cast<int64_t>(m) * N + n] = acc;
+        }
     }
     tc_fence_before();
     __syncthreads();
