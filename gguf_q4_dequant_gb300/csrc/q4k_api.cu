@@ -8,9 +8,8 @@
 //                   M >  16  -> K2 over consecutive 16-row slices of X
 //   q4k_matmul_bf16 M <= 16  -> K2 gemv_kernel (bf16 activations)
 //                   M >= 17  -> K3 gemm_kernel (tcgen05, TMEM accumulators)
-//   q4k_matmul_multi[_bf16]  -> the same, for up to 8 matrices sharing K and X:
-//                   one K2 launch for all of them (M <= 16), one K3 launch each
-//                   (M >= 17)
+//   q4k_matmul_multi[_bf16]  -> the same, for up to 8 matrices sharing K and X,
+//                   all of them in one launch (per 16-row slice for fp32 M > 16)
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -72,7 +71,7 @@ void init_device(int dev, DeviceState& st) {
     st.info.max_smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || gemv_setup() != cudaSuccess ||
-        gemm_setup() != cudaSuccess || encoder() == nullptr) {
+        gemm_setup(st.info) != cudaSuccess || encoder() == nullptr) {
         st.status = Q4K_ERR_CUDA;
         return;
     }
@@ -125,18 +124,25 @@ int encode_x_bf16(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN)
     return r == CUDA_SUCCESS ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
+// Tensor maps and the 128-row tile table of `count` matrices sharing K.
+int make_group(WeightGroup* grp, int count, const void* const* W, const int64_t* N, int64_t K) {
+    grp->count = count;
+    grp->tile_start[0] = 0;
+    for (int i = 0; i < count; ++i) {
+        const int rc = encode_w(&grp->maps[i], W[i], N[i], K, 128);
+        if (rc != Q4K_OK) return rc;
+        grp->N[i] = static_cast<int>(N[i]);
+        grp->tile_start[i + 1] = grp->tile_start[i] + static_cast<int>((N[i] + 127) / 128);
+    }
+    return Q4K_OK;
+}
+
 // One GEMV launch per 16-row slice of X over `count` matrices sharing K and X.
 int run_gemv(int count, const void* const* W, const int64_t* N, int64_t K, const void* X, bool xb,
              int64_t M, float* const* Y, cudaStream_t stream, const DeviceInfo& dev) {
-    GemvGroup grp;
-    grp.count = count;
-    grp.tile_start[0] = 0;
-    for (int i = 0; i < count; ++i) {
-        const int rc = encode_w(&grp.maps[i], W[i], N[i], K, 128);
-        if (rc != Q4K_OK) return rc;
-        grp.N[i] = static_cast<int>(N[i]);
-        grp.tile_start[i + 1] = grp.tile_start[i] + static_cast<int>((N[i] + 127) / 128);
-    }
+    WeightGroup grp;
+    const int rc = make_group(&grp, count, W, N, K);
+    if (rc != Q4K_OK) return rc;
     const size_t xelem = xb ? 2 : 4;
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int mc = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
@@ -149,17 +155,24 @@ int run_gemv(int count, const void* const* W, const int64_t* N, int64_t K, const
     return Q4K_OK;
 }
 
-int run_gemm(const void* W, int64_t N, int64_t K, const uint16_t* X, int64_t M, float* Y,
-             cudaStream_t stream, const DeviceInfo& dev) {
-    const GemmPlan plan =
-        gemm_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev.num_sms);
-    CUtensorMap tw, tx;
-    int rc;
-    if ((rc = encode_w(&tw, W, N, K, 128)) != Q4K_OK) return rc;
-    if ((rc = encode_x_bf16(&tx, X, M, K, plan.BN)) != Q4K_OK) return rc;
-    if (launch_gemm(tw, tx, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), Y, plan,
-                    stream, dev, g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
-        return Q4K_ERR_CUDA;
+// One GEMM launch over `count` matrices sharing K and X, per chunk of at most
+// 65535 * 32 rows of X (the grid's y limit at the narrowest tile).
+int run_gemm(int count, const void* const* W, const int64_t* N, int64_t K, const uint16_t* X,
+             int64_t M, float* const* Y, cudaStream_t stream, const DeviceInfo& dev) {
+    WeightGroup grp;
+    int rc = make_group(&grp, count, W, N, K);
+    if (rc != Q4K_OK) return rc;
+    constexpr int64_t kChunk = 65535LL * 32;
+    for (int64_t m0 = 0; m0 < M; m0 += kChunk) {
+        const int mc = static_cast<int>(M - m0 < kChunk ? M - m0 : kChunk);
+        const GemmPlan plan = gemm_plan(mc, grp.tile_start[count], static_cast<int>(K), dev);
+        CUtensorMap tx;
+        if ((rc = encode_x_bf16(&tx, X + m0 * K, mc, K, plan.BN)) != Q4K_OK) return rc;
+        for (int i = 0; i < count; ++i) grp.Y[i] = Y[i] + m0 * N[i];
+        if (launch_gemm(grp, tx, mc, static_cast<int>(K), plan, stream, dev,
+                        g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
+            return Q4K_ERR_CUDA;
+    }
     return Q4K_OK;
 }
 
@@ -237,7 +250,7 @@ int q4k_matmul_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16,
     if ((rc = current_device(&dev)) != Q4K_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M <= 16) return run_gemv(1, &W, &N, K, X_bf16, true, M, &Y, st, *dev);
-    return run_gemm(W, N, K, X_bf16, M, Y, st, *dev);
+    return run_gemm(1, &W, &N, K, X_bf16, M, &Y, st, *dev);
 }
 
 int q4k_matmul_multi(int count, const void* const* W, const int64_t* N, int64_t K, const float* X,
@@ -257,9 +270,7 @@ int q4k_matmul_multi_bf16(int count, const void* const* W, const int64_t* N, int
     if ((rc = current_device(&dev)) != Q4K_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M <= 16) return run_gemv(count, W, N, K, X_bf16, true, M, Y, st, *dev);
-    for (int i = 0; i < count; ++i)
-        if ((rc = run_gemm(W[i], N[i], K, X_bf16, M, Y[i], st, *dev)) != Q4K_OK) return rc;
-    return Q4K_OK;
+    return run_gemm(count, W, N, K, X_bf16, M, Y, st, *dev);
 }
 
 int q4k_set_pdl(int mode) {

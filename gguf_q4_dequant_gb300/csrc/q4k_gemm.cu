@@ -59,8 +59,9 @@ struct GemmCfg {
     static constexpr int kOffTmem = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffTmem + 16 + 1024;   // + alignment slack
     static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
-    // split-K slots: C <= 8 slots of BN x ceil(128 / C) floats in the A/B region
-    static_assert((kGemmBM + 8) * BN * 4 <= kOffW, "split-K slots must fit in the A/B region");
+    // split-K slots: C <= 8 slots of BN x rows floats in the A/B region, rows =
+    // ceil(128 / C) rounded up to a multiple of 4; C * rows <= 144 for C <= 8
+    static_assert((kGemmBM + 16) * BN * 4 <= kOffW, "split-K slots must fit in the A/B region");
 };
 
 // Eight weights of one nibble half (hh) from the qs word pair P = (w0, w1)
@@ -93,9 +94,8 @@ __device__ __forceinline__ uint4 dequant8x(uint64_t P, int hh, uint64_t d1s0, ui
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ CUtensorMap tmapX,
-                int M, int N, int K, float* __restrict__ Y, int C, int kb_per, int pdl_flags,
-                unsigned int* err) {
+    gemm_kernel(const __grid_constant__ WeightGroup grp, const __grid_constant__ CUtensorMap tmapX,
+                int M, int K, int C, int kb_per, int pdl_flags, unsigned int* err) {
     using Cfg = GemmCfg<BN>;
     constexpr int SA = Cfg::kAStages;
     constexpr int SB = Cfg::kBStages;
@@ -106,7 +106,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t sbase = raw + pad;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kGemmBM;
+    // global weight tile blockIdx.x -> (matrix, 128-row tile of it)
+    const int mi = group_matrix(grp, blockIdx.x);
+    const CUtensorMap* tmapW = &grp.maps[mi];
+    const int N = grp.N[mi];
+    float* __restrict__ Y = grp.Y[mi];
+    const int n0 = (blockIdx.x - grp.tile_start[mi]) * kGemmBM;
     const int m0 = blockIdx.y * BN;
     const int rank = blockIdx.z;  // cluster rank along z = K-slice
     const int kb0 = rank * kb_per;
@@ -159,7 +164,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ---
         if (lane == 0) {
-            tma_prefetch_desc(&tmapW);
+            tma_prefetch_desc(tmapW);
             tma_prefetch_desc(&tmapX);
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int ws = sb % kGemmWStages;
                     if (mbar_test_wait(bw_empty + 8 * ws, ((sb / kGemmWStages) & 1) ^ 1)) {
                         mbar_arrive_expect_tx(bw_full + 8 * ws, kGemmWStageBytes);
-                        tma_load_2d_hint(sbase + Cfg::kOffW + ws * kGemmWStageBytes, &tmapW,
+                        tma_load_2d_hint(sbase + Cfg::kOffW + ws * kGemmWStageBytes, tmapW,
                                          (kb0 + sb) * kBlockBytes, n0, bw_full + 8 * ws, pol_w);
                         ++sb;
                         progress = true;
@@ -302,13 +307,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     }
     if (C > 1) {
-        // Split K: rank r owns rows [r*rows, r*rows + nr) of the tile. Once
+        // Split K: rank r owns rows [r*rows, min(128, (r+1)*rows)) of the tile. Once
         // every CTA's MMAs are complete (first cluster barrier) the A/B region
         // of every CTA is free, and each CTA pushes the rows it does not own
         // straight from TMEM into the owner's region (posted remote stores:
         // slot [source rank][column][owned row]); after the second barrier
         // each owner adds the C slots in rank order (deterministic).
-        const int rows = (kGemmBM + C - 1) / C;
+        const int rows = ((kGemmBM + C - 1) / C + 3) & ~3;  // a multiple of 4 (float4 groups)
         const uint32_t slot_bytes = 4u * static_cast<uint32_t>(BN * rows);
         const uint32_t pbase = sbase + Cfg::kOffA;
         cluster_sync_all();
@@ -330,15 +335,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         cluster_sync_all();
         const int r0 = rank * rows;
-        const int nr = min(kGemmBM, r0 + rows) - r0;
+        const int nr4 = (min(kGemmBM, r0 + rows) - r0) >> 2;  // owned rows / 4 (> 0 for C <= 8)
         const float* part = reinterpret_cast<const float*>(smem + Cfg::kOffA);
-        for (int idx = threadIdx.x; idx < nr * BN; idx += kGemmThreads) {
-            const int col = idx / nr;
-            const int rl = idx - col * nr;
-            float acc = 0.f;
-            for (int src = 0; src < C; ++src) acc += part[src * (BN * rows) + col * rows + rl];
+        const bool vec = (N & 3) == 0;  // Y rows 16-byte aligned
+        for (int idx = threadIdx.x; idx < nr4 * BN; idx += kGemmThreads) {
+            const int col = idx / nr4;
+            const int rl = 4 * (idx - col * nr4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int src = 0; src < C; ++src) {
+                const float4 v = *reinterpret_cast<const float4*>(part + src * (BN * rows) + col * rows + rl);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
             const int n = n0 + r0 + rl, m = m0 + col;
-            if (n < N && m < M) Y[static_cast<int64_t>(m) * N + n] = acc;
+            if (m >= M) continue;
+            float* y = Y + static_cast<int64_t>(m) * N + n;
+            if (vec && n + 3 < N) {
+                *reinterpret_cast<float4*>(y) = acc;
+            } else {
+                if (n < N) y[0] = acc.x;
+                if (n + 1 < N) y[1] = acc.y;
+                if (n + 2 < N) y[2] = acc.z;
+                if (n + 3 < N) y[3] = acc.w;
+            }
         }
     }
     tc_fence_before();
@@ -351,29 +372,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------------------ host ---
 
-// Tile width BN (tokens) and K-split C for an M x N x K product, from a
-// wave-count cost model: a CTA spends max(2*BN, 300) cycles per 64-k step (the
-// MMA of a 128 x BN x 64 step versus the dequantising warps), plus ~2000 cycles
-// of prologue and pipeline fill and its epilogue (~4000 more with a split).
-GemmPlan gemm_plan(int M, int N, int K, int num_sms) {
+// Tile width BN (tokens) and K-split C for M token rows over `ntiles` 128-row
+// weight tiles, from a cost model fitted to measurements of this kernel: a CTA
+// costs ~4 us of launch, pipeline fill and epilogue plus ~0.38 us per 64-k
+// step whatever BN is (the dequantising warps set the pace), and a K-split adds
+// the DSMEM reduction (~0.5 us + 0.018 us per token column, twice that above
+// four ranks). Waves come from the number of clusters the occupancy API says
+// can be resident at once.
+GemmPlan gemm_plan(int M, int ntiles, int K, const DeviceInfo& dev) {
     const int KB = K / kBlockWeights;
-    const int ntiles = (N + kGemmBM - 1) / kGemmBM;
-    const int bns[2] = {M <= 32 ? 32 : M <= 64 ? 64 : 128, M > 128 ? 256 : 0};
     const int cs[6] = {1, 2, 3, 4, 6, 8};
-    GemmPlan best{bns[0], 1, KB};
+    GemmPlan best{32, 1, KB};
     double best_cost = 1e300;
-    for (int bn : bns) {
-        if (bn == 0) continue;
+    for (int bi = 0; bi < 4; ++bi) {
+        const int bn = 32 << bi;
+        if (bn > 32 && bn / 2 >= M) break;  // a narrower tile already covers M
         const int mtiles = (M + bn - 1) / bn;
         for (int c : cs) {
             if (c > KB) break;
             const int kb_per = (KB + c - 1) / c;
             const int ce = (KB + kb_per - 1) / kb_per;
-            const long ctas = static_cast<long>(ntiles) * mtiles * ce;
-            const long waves = (ctas + num_sms - 1) / num_sms;
-            const double tk = 2.0 * bn > 300.0 ? 2.0 * bn : 300.0;
-            const double cost = static_cast<double>(waves) *
-                                (4.0 * kb_per * tk + 2000.0 + (ce > 1 ? 4000.0 + 8.0 * bn : 4.0 * bn));
+            const int resident = dev.gemm_clusters[bi][ce];
+            if (resident < 1) continue;
+            const long clusters = static_cast<long>(ntiles) * mtiles;
+            const long waves = (clusters + resident - 1) / resident;
+            double per = 4.0 + 0.38 * 4.0 * kb_per;
+            if (ce > 1) per += (0.5 + 0.018 * bn) * (ce <= 4 ? 1.0 : 2.0);
+            const double cost = static_cast<double>(waves) * per;
             if (cost < best_cost * 0.999) {
                 best_cost = cost;
                 best = GemmPlan{bn, ce, kb_per};
@@ -384,26 +409,46 @@ GemmPlan gemm_plan(int M, int N, int K, int num_sms) {
 }
 
 template <int BN>
-static cudaError_t set_attr() {
-    return cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                GemmCfg<BN>::kSmem);
+static cudaError_t setup_bn(DeviceInfo& dev, int bi) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GemmCfg<BN>::kSmem);
+    if (e != cudaSuccess) return e;
+    for (int c = 1; c <= 8; ++c) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, c);
+        cfg.blockDim = dim3(kGemmThreads, 1, 1);
+        cfg.dynamicSmemBytes = GemmCfg<BN>::kSmem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 1;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = c;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN>, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = c == 1 ? dev.num_sms : 0;  // plain launches need no co-scheduling
+        }
+        dev.gemm_clusters[bi][c] = n;
+    }
+    return cudaSuccess;
 }
 
-cudaError_t gemm_setup() {
+cudaError_t gemm_setup(DeviceInfo& dev) {
     cudaError_t e = cudaSuccess, r;
-    if ((r = set_attr<32>()) != cudaSuccess) e = r;
-    if ((r = set_attr<64>()) != cudaSuccess) e = r;
-    if ((r = set_attr<128>()) != cudaSuccess) e = r;
-    if ((r = set_attr<256>()) != cudaSuccess) e = r;
+    if ((r = setup_bn<32>(dev, 0)) != cudaSuccess) e = r;
+    if ((r = setup_bn<64>(dev, 1)) != cudaSuccess) e = r;
+    if ((r = setup_bn<128>(dev, 2)) != cudaSuccess) e = r;
+    if ((r = setup_bn<256>(dev, 3)) != cudaSuccess) e = r;
     return e;
 }
 
 template <int BN>
-static cudaError_t launch_bn(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                             float* Y, const GemmPlan& plan, cudaStream_t stream, unsigned int* err,
-                             int pdl) {
+static cudaError_t launch_bn(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K,
+                             const GemmPlan& plan, cudaStream_t stream, unsigned int* err, int pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + kGemmBM - 1) / kGemmBM, (M + BN - 1) / BN, plan.C);
+    cfg.gridDim = dim3(grp.tile_start[grp.count], (M + BN - 1) / BN, plan.C);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = GemmCfg<BN>::kSmem;
     cfg.stream = stream;
@@ -424,18 +469,17 @@ static cudaError_t launch_bn(const CUtensorMap& tmapW, const CUtensorMap& tmapX,
     cfg.attrs = attr;
     cfg.numAttrs = na;
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, tmapW, tmapX, M, N, K, Y, plan.C, plan.kb_per,
-                              pdl_flags, err);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, grp, tmapX, M, K, plan.C, plan.kb_per, pdl_flags,
+                              err);
 }
 
-cudaError_t launch_gemm(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                        float* Y, const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev,
-                        int pdl) {
+cudaError_t launch_gemm(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K,
+                        const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev, int pdl) {
     switch (plan.BN) {
-        case 32: return launch_bn<32>(tmapW, tmapX, M, N, K, Y, plan, stream, dev.err, pdl);
-        case 64: return launch_bn<64>(tmapW, tmapX, M, N, K, Y, plan, stream, dev.err, pdl);
-        case 128: return launch_bn<128>(tmapW, tmapX, M, N, K, Y, plan, stream, dev.err, pdl);
-        case 256: return launch_bn<256>(tmapW, tmapX, M, N, K, Y, plan, stream, dev.err, pdl);
+        case 32: return launch_bn<32>(grp, tmapX, M, K, plan, stream, dev.err, pdl);
+        case 64: return launch_bn<64>(grp, tmapX, M, K, plan, stream, dev.err, pdl);
+        case 128: return launch_bn<128>(grp, tmapX, M, K, plan, stream, dev.err, pdl);
+        case 256: return launch_bn<256>(grp, tmapX, M, K, plan, stream, dev.err, pdl);
     }
     return cudaErrorInvalidValue;
 }

@@ -235,16 +235,10 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
 // Grid: gridDim.x = (number of clusters) * C; a cluster of C CTAs along x
 // shares tiles and splits K into C slices of kb_per super-blocks. With C > 1
 // every cluster owns exactly one tile.
-// Matrix of the group that owns global tile t.
-__device__ __forceinline__ int group_matrix(const GemvGroup& g, int t) {
-    int i = 0;
-    while (i + 1 < g.count && t >= g.tile_start[i + 1]) ++i;
-    return i;
-}
 
 template <int MT, bool XB>
 __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks)
-    gemv_kernel(const __grid_constant__ GemvGroup grp, const void* __restrict__ X, int M, int K,
+    gemv_kernel(const __grid_constant__ WeightGroup grp, const void* __restrict__ X, int M, int K,
                 int C, int kb_per, int pdl_flags, unsigned int* err) {
     using Cfg = GemvCfg<MT>;
     constexpr int S = Cfg::kStages;
@@ -471,7 +465,7 @@ cudaError_t gemv_setup() {
 }
 
 template <int MT, bool XB>
-static cudaError_t launch_mt(const GemvGroup& grp, const void* X, int M, int K, cudaStream_t stream,
+static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K, cudaStream_t stream,
                              const DeviceInfo& dev, int slot, int pdl) {
     const int KB = K / kBlockWeights;
     const int tiles = grp.tile_start[grp.count];
@@ -517,7 +511,7 @@ static cudaError_t launch_mt(const GemvGroup& grp, const void* X, int M, int K, 
     return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, XB>, grp, X, M, K, C, kb_per, pdl_flags, dev.err);
 }
 
-cudaError_t launch_gemv(const GemvGroup& grp, const void* X, bool x_bf16, int M, int K,
+cudaError_t launch_gemv(const WeightGroup& grp, const void* X, bool x_bf16, int M, int K,
                         cudaStream_t stream, const DeviceInfo& dev, int pdl) {
     const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
 #define Q4K_CASE(MT, SLOT)                                                            \

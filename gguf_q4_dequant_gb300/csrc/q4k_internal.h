@@ -12,6 +12,9 @@ struct DeviceInfo {
     int num_sms = 0;
     int max_smem_optin = 0;
     unsigned int* err = nullptr;  // device address of the device error word
+    // GEMM: clusters of C CTAs that can be resident at once, per tile width
+    // BN = 32 << i (i < 4) and split C (index C, 1..8), from the occupancy API.
+    int gemm_clusters[4][9] = {};
 };
 
 cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, cudaStream_t stream,
@@ -24,29 +27,39 @@ cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, c
 // Split-K GEMV for 1 <= M <= 16 rows of activations (fp32 or bf16 bit patterns)
 // over up to kMaxGroup weight matrices that share K and X (one launch).
 constexpr int kMaxGroup = 8;
-struct alignas(64) GemvGroup {
+// Up to kMaxGroup weight matrices that share K and X, as one launch: global
+// 128-row tile t belongs to matrix i with tile_start[i] <= t < tile_start[i+1].
+struct alignas(64) WeightGroup {
     CUtensorMap maps[kMaxGroup];     // W_i: 2-D uint8 map {K/256*144, N_i}, box {144, 128}
     float* Y[kMaxGroup];             // Y_i: fp32 [M][N_i]
     int N[kMaxGroup];
     int tile_start[kMaxGroup + 1];   // prefix sums of ceil(N_i / 128)
     int count;
 };
-cudaError_t launch_gemv(const GemvGroup& grp, const void* X, bool x_bf16, int M, int K,
+
+// Matrix of the group that owns global tile t.
+__host__ __device__ inline int group_matrix(const WeightGroup& g, int t) {
+    int i = 0;
+    while (i + 1 < g.count && t >= g.tile_start[i + 1]) ++i;
+    return i;
+}
+cudaError_t launch_gemv(const WeightGroup& grp, const void* X, bool x_bf16, int M, int K,
                         cudaStream_t stream, const DeviceInfo& dev, int pdl);
 cudaError_t gemv_setup();
 
-// tcgen05 GEMM for M >= 17 rows of bf16 activations.
-// tmapW: 2-D uint8 map {K/256*144, N}, box {144, 128}; tmapX: 2-D bf16 map
-// {K, M}, box {64, BN}, 128-byte swizzle.
+// tcgen05 GEMM for M >= 17 rows of bf16 activations over a group of weight
+// matrices (grp.maps as for the GEMV); tmapX: 2-D bf16 map {K, M}, box
+// {64, BN}, 128-byte swizzle.
 struct GemmPlan {
     int BN;      // tokens per tile (MMA N)
     int C;       // K-split factor (cluster size along z)
     int kb_per;  // super-blocks per K-slice
 };
-GemmPlan gemm_plan(int M, int N, int K, int num_sms);
-cudaError_t launch_gemm(const CUtensorMap& tmapW, const CUtensorMap& tmapX, int M, int N, int K,
-                        float* Y, const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev,
-                        int pdl);
-cudaError_t gemm_setup();
+// ntiles: total 128-row weight tiles of the group.
+GemmPlan gemm_plan(int M, int ntiles, int K, const DeviceInfo& dev);
+cudaError_t launch_gemm(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K,
+                        const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev, int pdl);
+// Sets the kernels' attributes and fills dev.gemm_clusters.
+cudaError_t gemm_setup(DeviceInfo& dev);
 
 }  // namespace q4k

@@ -102,9 +102,10 @@ int q4k_matmul_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16,
  * all W_i have the same K and take the same activations X -- e.g. the q, k and
  * v projections of a layer, or its gate and up projections. W, N and Y are
  * host arrays of length count holding device pointers / row counts; Y_i is
- * fp32 [M][N_i]. For M <= 16 all matrices run in one launch (accuracy as
- * q4k_matmul / q4k_matmul_bf16); for larger M each matrix is its own call.
- * The same checks as the single calls apply to every matrix.
+ * fp32 [M][N_i]. All matrices run in one launch (fp32 activations with
+ * M > 16: one launch per 16-row slice of X), with the kernel and accuracy of
+ * q4k_matmul / q4k_matmul_bf16 for the same M. The same checks as the single
+ * calls apply to every matrix.
  */
 int q4k_matmul_multi(int count, const void* const* W, const int64_t* N, int64_t K, const float* X,
                      int64_t M, float* const* Y, void* stream);

@@ -320,7 +320,7 @@ def test_grouped_matmul(q4k, oracle_mod, xdt):
     Whs = [synth.weight_rows(8000 + i, n, K) for i, n in enumerate(Ns)]
     Wds = [w.to(DEV) for w in Whs]
     dt = torch.bfloat16 if xdt == "bf16" else torch.float32
-    Ms = (1, 3, 16, 40) if xdt == "bf16" else (1, 3, 16, 20)
+    Ms = (1, 3, 16, 40, 300) if xdt == "bf16" else (1, 3, 16, 20)
     for M in Ms:
         X = synth.activations(8100 + M, M, K, dt)
         Ys = [torch.full((M, n), float("nan"), device=DEV) for n in Ns]
@@ -333,6 +333,31 @@ def test_grouped_matmul(q4k, oracle_mod, xdt):
             got = Y.cpu().double().numpy()
             assert np.all(np.isfinite(got))
             assert float(np.max(np.abs(got - Yref) / (tol * A + 1e-30))) <= 1.0
+
+
+def test_grouped_gemm_eight_matrices(q4k, oracle_mod):
+    """The largest group through the tensor-core GEMM (one launch, global tile
+    index -> matrix), twice in a row: results within the GEMM bar and identical."""
+    K = 768
+    Ns = [128, 1, 129, 640, 255, 384, 16, 1000]
+    Whs = [synth.weight_rows(8400 + i, n, K) for i, n in enumerate(Ns)]
+    Wds = [w.to(DEV) for w in Whs]
+    M = 200
+    X = synth.activations(8500, M, K, torch.bfloat16)
+    Xd = X.to(DEV)
+    runs = []
+    for _ in range(2):
+        Ys = [torch.full((M, n), float("nan"), device=DEV) for n in Ns]
+        q4k.q4k_matmul_multi(Wds, Ns, K, Xd, M, Ys)
+        torch.cuda.synchronize()
+        runs.append([y.cpu() for y in Ys])
+    Xo = _x_for_oracle(oracle_mod, X)
+    for Wh, n, a, b in zip(Whs, Ns, runs[0], runs[1]):
+        assert torch.equal(a, b)
+        Yref, A = oracle_mod.matmul(Wh.numpy(), n, K, Xo)
+        got = a.double().numpy()
+        assert np.all(np.isfinite(got))
+        assert float(np.max(np.abs(got - Yref) / (TOL_GEMM * A + 1e-30))) <= 1.0
 
 
 def test_grouped_matmul_in_graph_with_pdl(q4k):
