@@ -44,8 +44,10 @@ def _peaks():
 
 
 KERNEL_SOURCES = {
-    "gemv_kernel<1,f32>": ["gguf_q4_dequant_gb300/csrc/q4k_gemv.cu", "gguf_q4_dequant_gb300/csrc/q4k_device.cuh"],
-    "gemm_kernel<256>": ["gguf_q4_dequant_gb300/csrc/q4k_gemm.cu", "gguf_q4_dequant_gb300/csrc/q4k_device.cuh"],
+    "gemv_kernel<1,f32>": ["gguf_q4_dequant_gb300/csrc/q4k_gemv.cu", "gguf_q4_dequant_gb300/csrc/q4k_device.cuh",
+                           "gguf_q4_dequant_gb300/csrc/q4k_internal.h"],
+    "gemm_kernel": ["gguf_q4_dequant_gb300/csrc/q4k_gemm.cu", "gguf_q4_dequant_gb300/csrc/q4k_device.cuh",
+                    "gguf_q4_dequant_gb300/csrc/q4k_internal.h"],
 }
 
 
@@ -490,7 +492,7 @@ def run_gpu(args):
                          "frac": round(achieved3 / bf16_peak, 4),
                          "frac_of_sustained": round(achieved3 / bf16_sust, 4) if bf16_sust else None,
                          "peak_source": f"{peak_kind} bf16_tflops (cuBLAS burst)",
-                         "traffic": measured_traffic("gemm_kernel<256>"),
+                         "traffic": measured_traffic("gemm_kernel"),
                          "avg_launch_us": round(gemm_ms * 1e3, 2),
                          "avg_launch_basis": "CUDA-graph sweep time / launches (gaps included)"}}
         out["_flops3"] = flops3

@@ -16,12 +16,12 @@
 //   group     = up to 8 weight matrices that share K and the activations (q, k
 //               and v of a layer; gate and up) are one launch: their tiles are
 //               numbered consecutively and each has its own TMA map and output.
-//   CTA       = consumer warps in G groups of 4 (warp w of a group owns rows
-//               32w..32w+31 of the tile, one lane per row); every group works
-//               on every stage, group g taking chunks [4g/G, 4(g+1)/G) of each
-//               row's super-block, and the groups add their sums once per
-//               tile. Plus 1 TMA producer warp and 1 activation warp. CTAs are
-//               persistent over tiles, so the stage ring streams continuously.
+//   CTA       = 4 consumer warps (warp w owns rows 32w..32w+31 of the tile,
+//               one lane per row and the whole super-block of that row per
+//               stage, so the per-stage and per-super-block set-up -- barrier
+//               waits, scale unpacking -- is paid once per 256 weights), 1 TMA
+//               producer warp and 1 activation warp. CTAs are persistent over
+//               tiles, so the stage ring streams continuously.
 //
 // Per-weight arithmetic (the unpack happens in registers):
 //   A 4-bit quant q left in place inside its 32-bit word at bit 4p (p = 0..4)
@@ -43,15 +43,12 @@
 namespace q4k {
 
 constexpr int kGemvTileRows = 128;
-constexpr int kGemvGroupWarps = 4;     // one consumer group covers the 128-row tile
+constexpr int kGemvConsumers = 4;  // consumer warps: one lane per row of the tile
 constexpr int kGemvStageBytes = kGemvTileRows * kBlockBytes;  // 18432
 
 template <int MT>
 struct GemvCfg {
-    // two consumer groups (each half of every super-block) for small M; one
-    // group for M >= 8, whose register footprint leaves no room for a second
-    static constexpr int kGroups = MT >= 8 ? 1 : 2;
-    static constexpr int kConsumers = kGroups * kGemvGroupWarps;
+    static constexpr int kConsumers = kGemvConsumers;
     static constexpr int kProducerWarp = kConsumers;
     static constexpr int kStagerWarp = kConsumers + 1;
     static constexpr int kThreads = 32 * (kConsumers + 2);
@@ -64,8 +61,7 @@ struct GemvCfg {
     static constexpr int kOffXs = kOffX + kStages * MT * 256 * 4;        // sums [stage][m][8]
     static constexpr int kOffInv = kOffXs + kStages * MT * 8 * 4;        // 2^-E [stage][m][2]
     static constexpr int kOffRed = kOffInv + kStages * MT * 2 * 4;       // ranks 1..7: [7][m][128]
-    static constexpr int kOffGrp = kOffRed + 7 * MT * kGemvTileRows * 4; // group-1 sums [2][m][128]
-    static constexpr int kOffBar = kOffGrp + 2 * MT * kGemvTileRows * 4; // full[S], empty[S], red
+    static constexpr int kOffBar = kOffRed + 7 * MT * kGemvTileRows * 4; // full[S], empty[S], red
     static constexpr int kSmem = kOffBar + (2 * kStages + 1) * 8 + 128;  // + alignment slack
 };
 
@@ -160,8 +156,7 @@ struct XPrefetch {
 };
 // One consumer lane: the contribution of one super-block of its row, scaled by
 // 2^E (acc[m] for each activation row m).
-// Chunks C0 .. C0+NC-1 (sub-blocks 2*C0 .. 2*(C0+NC)-1) of the super-block.
-template <int MT, int C0, int NC>
+template <int MT>
 __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, const float* xsum,
                                           float (&acc)[MT]) {
     const uint4 h = *reinterpret_cast<const uint4*>(P);
@@ -170,7 +165,7 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
     uint64_t dsc[8];  // (d*sc_j, d*sc_j) pairs
     float mm[8];      // dmin*m_j
 #pragma unroll
-    for (int j = 2 * C0; j < 2 * (C0 + NC); ++j) {
+    for (int j = 0; j < 8; ++j) {
         const uint32_t scw = j < 4 ? sb.sc_lo : sb.sc_hi;
         const uint32_t mw = j < 4 ? sb.m_lo : sb.m_hi;
         const float a = d * byte_to_float(scw, j & 3);
@@ -181,7 +176,7 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
 #pragma unroll
     for (int m = 0; m < MT; ++m) tot[m] = 0ull;
 #pragma unroll
-    for (int c = C0; c < C0 + NC; ++c) {
+    for (int c = 0; c < 4; ++c) {
         // the 32 qs bytes of chunk c as four word pairs (u, u+1)
         const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c);
         const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(P + 32 + 32 * c);
@@ -226,7 +221,7 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
         const float* xsm = xsum + m * 8;
         float mins = 0.f;
 #pragma unroll
-        for (int j = 2 * C0; j < 2 * (C0 + NC); ++j) mins = fmaf(mm[j], xsm[j], mins);
+        for (int j = 0; j < 8; ++j) mins = fmaf(mm[j], xsm[j], mins);
         const float2 t = unpack2(tot[m]);
         acc[m] = (t.x + t.y) - mins;
     }
@@ -270,7 +265,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             mbar_init(bar_empty + 8 * s, Cfg::kConsumers);  // every consumer warp reads every stage
         }
         // rank 0 of a cluster: the other ranks' group-0 consumer threads
-        mbar_init(bar_red, C > 1 ? (C - 1) * 32 * kGemvGroupWarps : 1);
+        mbar_init(bar_red, C > 1 ? (C - 1) * 32 * kGemvConsumers : 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -347,9 +342,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     } else {
         // ------------------------------------------------------- consumers ---
         pdl_wait();  // before any global write
-        const int g = warp / kGemvGroupWarps;                     // group: chunk range of every stage
-        const int r = 32 * (warp % kGemvGroupWarps) + lane;       // row within the tile
-        float* gsum = reinterpret_cast<float*>(smem + Cfg::kOffGrp);
+        const int r = 32 * warp + lane;  // row within the tile
         float y[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) y[m] = 0.f;
@@ -364,12 +357,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                     const uint8_t* P = smem + Cfg::kOffW + s * kGemvStageBytes + r * kBlockBytes;
                     const float* xs = xs_ring + s * MT * 256;
                     const float* xsm = xsum_ring + s * MT * 8;
-                    if constexpr (Cfg::kGroups == 1) {
-                        block_dot<MT, 0, 4>(P, xs, xsm, acc);
-                    } else {
-                        if (g == 0) block_dot<MT, 0, 2>(P, xs, xsm, acc);
-                        else block_dot<MT, 2, 2>(P, xs, xsm, acc);
-                    }
+                    block_dot<MT>(P, xs, xsm, acc);
                     const float* inv = inv_ring + s * MT * 2;
 #pragma unroll
                     for (int m = 0; m < MT; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
@@ -377,38 +365,20 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             }
-            // tile done: group 1 hands its sums to group 0 (double-buffered by tile parity)
-            float* gbuf = gsum + (i & 1) * MT * kGemvTileRows;
-            if constexpr (Cfg::kGroups == 2) {
-                if (g == 1) {
+            if (C == 1) {  // C > 1: one tile per CTA, reduced across the cluster below
+                const int t = cid + i * ncl;
+                const int mi = group_matrix(grp, t);
+                const int row = (t - grp.tile_start[mi]) * kGemvTileRows + r;
+                const int Nm = grp.N[mi];
+                float* Ym = grp.Y[mi];
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        gbuf[m * kGemvTileRows + r] = y[m];
-                        y[m] = 0.f;
-                    }
-                }
-                named_bar_sync(1, 32 * Cfg::kConsumers);
-            }
-            if (g == 0) {
-                if constexpr (Cfg::kGroups == 2) {
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) y[m] += gbuf[m * kGemvTileRows + r];
-                }
-                if (C == 1) {  // C > 1: one tile per CTA, reduced across the cluster below
-                    const int t = cid + i * ncl;
-                    const int mi = group_matrix(grp, t);
-                    const int row = (t - grp.tile_start[mi]) * kGemvTileRows + r;
-                    const int Nm = grp.N[mi];
-                    float* Ym = grp.Y[mi];
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        if (m < M && row < Nm) Ym[static_cast<int64_t>(m) * Nm + row] = y[m];
-                        y[m] = 0.f;
-                    }
+                for (int m = 0; m < MT; ++m) {
+                    if (m < M && row < Nm) Ym[static_cast<int64_t>(m) * Nm + row] = y[m];
+                    y[m] = 0.f;
                 }
             }
         }
-        if (C > 1 && g == 0) {
+        if (C > 1) {
             // K-slices of this cluster's tile: ranks 1.. push into rank 0, which adds in rank order
             cluster_wait();
             if (rank != 0) {

@@ -29,7 +29,7 @@ cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, c
 constexpr int kMaxGroup = 8;
 // Up to kMaxGroup weight matrices that share K and X, as one launch: global
 // 128-row tile t belongs to matrix i with tile_start[i] <= t < tile_start[i+1].
-struct alignas(64) WeightGroup {
+struct WeightGroup {  // aligned as its CUtensorMap members
     CUtensorMap maps[kMaxGroup];     // W_i: 2-D uint8 map {K/256*144, N_i}, box {144, 128}
     float* Y[kMaxGroup];             // Y_i: fp32 [M][N_i]
     int N[kMaxGroup];
