@@ -442,9 +442,11 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
     const int slots = dev.num_sms * g_occ[XB ? 1 : 0][slot];
     int C = 1, kb_per = KB, grid;
     if (tiles >= slots) {
-        // persistent: every CTA streams the same number of tiles (+-1)
-        const int waves = (tiles + slots - 1) / slots;
-        grid = (tiles + waves - 1) / waves;
+        // persistent, one CTA per resident slot (CTA c streams tiles c, c + grid,
+        // ...): the busiest SM then holds ceil(tiles / SMs) tiles, where sizing the
+        // grid to equalise tiles per CTA would leave some SMs with one CTA and
+        // others with two full ones
+        grid = slots;
     } else {
         // split K across a cluster (at most 8 CTAs, at least one super-block each)
         C = slots / tiles;
