@@ -60,8 +60,11 @@ struct GemvCfg {
     static constexpr int kOffX = kOffW + kStages * kGemvStageBytes;     // x' [stage][m][256]
     static constexpr int kOffXs = kOffX + kStages * MT * 256 * 4;        // sums [stage][m][8]
     static constexpr int kOffInv = kOffXs + kStages * MT * 8 * 4;        // 2^-E [stage][m][2]
-    static constexpr int kOffRed = kOffInv + kStages * MT * 2 * 4;       // ranks 1..7: [7][m][128]
-    static constexpr int kOffBar = kOffRed + 7 * MT * kGemvTileRows * 4; // full[S], empty[S], red
+    // K-split across a cluster of at most kMaxSplit CTAs (16 is a non-portable
+    // cluster size, used only where its reduction slots stay small)
+    static constexpr int kMaxSplit = MT <= 2 ? 16 : 8;
+    static constexpr int kOffRed = kOffInv + kStages * MT * 2 * 4;       // ranks 1..: [kMaxSplit-1][m][128]
+    static constexpr int kOffBar = kOffRed + (kMaxSplit - 1) * MT * kGemvTileRows * 4;  // full[S], empty[S], red
     static constexpr int kSmem = kOffBar + (2 * kStages + 1) * 8 + 128;  // + alignment slack
 };
 
@@ -408,7 +411,8 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
 // ------------------------------------------------------------------ host ---
 
 namespace {
-int g_occ[2][5];  // resident CTAs per SM for each (XB, MT) instantiation
+int g_occ[2][5];           // resident CTAs per SM for each (XB, MT) instantiation
+int g_clusters[2][5][17];  // resident clusters of C CTAs (C = 2..kMaxSplit), same index
 }
 
 template <int MT, bool XB>
@@ -420,7 +424,31 @@ static cudaError_t set_attr(int slot) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<MT, XB>, GemvCfg<MT>::kThreads,
                                                       GemvCfg<MT>::kSmem);
     g_occ[XB ? 1 : 0][slot] = occ < 1 ? 1 : occ;
-    return e;
+    if (e != cudaSuccess) return e;
+    if (GemvCfg<MT>::kMaxSplit > 8 &&
+        cudaFuncSetAttribute(gemv_kernel<MT, XB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+        (void)cudaGetLastError();  // then the occupancy query below reports 0 for C > 8
+    for (int c = 2; c <= GemvCfg<MT>::kMaxSplit; ++c) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c, 1, 1);
+        cfg.blockDim = dim3(GemvCfg<MT>::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = GemvCfg<MT>::kSmem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = c;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<MT, XB>, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        g_clusters[XB ? 1 : 0][slot][c] = n;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t gemv_setup() {
@@ -448,12 +476,21 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
         // others with two full ones
         grid = slots;
     } else {
-        // split K across a cluster (at most 8 CTAs, at least one super-block each)
-        C = slots / tiles;
-        C = C < 1 ? 1 : (C > 8 ? 8 : C);
-        C = C > KB ? KB : C;
-        kb_per = (KB + C - 1) / C;
-        C = (KB + kb_per - 1) / kb_per;
+        // split K across a cluster (at least one super-block per CTA), as wide
+        // as the CTA slots allow while every cluster is resident at once
+        int c = slots / tiles;
+        c = c > GemvCfg<MT>::kMaxSplit ? GemvCfg<MT>::kMaxSplit : c;
+        c = c > KB ? KB : c;
+        C = 1;
+        for (; c >= 2; --c) {
+            const int kp = (KB + c - 1) / c;
+            const int ce = (KB + kp - 1) / kp;
+            if (g_clusters[XB ? 1 : 0][slot][ce] >= tiles) {
+                C = ce;
+                kb_per = kp;
+                break;
+            }
+        }
         grid = tiles * C;
     }
     cudaLaunchConfig_t cfg = {};
