@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             mbar_init(bar_full + 8 * s, 1 + 32);  // producer (with bytes) + 32 activation lanes
             mbar_init(bar_empty + 8 * s, Cfg::kConsumers);  // every consumer warp reads every stage
         }
-        // rank 0 of a cluster: the other ranks' group-0 consumer threads
-        mbar_init(bar_red, C > 1 ? (C - 1) * 32 * kGemvConsumers : 1);
+        // rank 0 of a cluster: one arrival per consumer warp of every other rank
+        mbar_init(bar_red, C > 1 ? (C - 1) * kGemvConsumers : 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -388,7 +388,9 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 const uint32_t dst = map_shared_rank(smem_u32(red + (rank - 1) * MT * kGemvTileRows), 0);
 #pragma unroll
                 for (int m = 0; m < MT; ++m) st_shared_cluster_f32(dst + 4 * (m * kGemvTileRows + r), y[m]);
-                mbar_arrive_remote(map_shared_rank(bar_red, 0));
+                // the warp's stores are ordered before lane 0's release-arrive
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(map_shared_rank(bar_red, 0));
             } else if (mbar_wait(bar_red, 0, err)) {
                 const int mi = group_matrix(grp, cid);
                 const int row = (cid - grp.tile_start[mi]) * kGemvTileRows + r;
