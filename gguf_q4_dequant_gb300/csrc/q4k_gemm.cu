@@ -248,34 +248,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int sb = 0; sb < KB && ok; ++sb) {
             const int ws = sb % kGemmWStages;
             if (!mbar_wait(bw_full + 8 * ws, (sb / kGemmWStages) & 1, err)) { ok = false; break; }
+            // everything this thread needs from the packed super-block (its
+            // 4 x 16 qs bytes and the 8 scale factors) is read into registers
+            // at once and the W stage released, so the per-step chain below
+            // holds no shared-memory load
             const uint8_t* P = smem + Cfg::kOffW + ws * kGemmWStageBytes + r * kBlockBytes;
             const uint4 hd = *reinterpret_cast<const uint4*>(P);
+            ulonglong2 qv[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) qv[c] = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c + 16 * p);
+            mbar_arrive(bw_empty + 8 * ws);
             const ScaleBytes scb = decode_scales(hd.y, hd.z, hd.w);
             const float d = half_lo(hd.x), dmin = half_hi(hd.x);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int ks = sb * 4 + c;
                 const int s = ks % SA;
-                if (!mbar_wait(ba_empty + 8 * s, ((ks / SA) & 1) ^ 1, err)) { ok = false; break; }
                 const int j = 2 * c + hh;  // sub-block
                 const uint32_t scw = j < 4 ? scb.sc_lo : scb.sc_hi;
                 const uint32_t mw = j < 4 ? scb.m_lo : scb.m_hi;
                 const float d1 = d * byte_to_float(scw, j & 3);
                 const float m1 = dmin * byte_to_float(mw, j & 3);
                 const float d1s0 = d1 * exp2i(-4 * hh), d1s1 = d1 * exp2i(-8 - 4 * hh);
-                const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c + 16 * p);
+                const uint64_t D0 = pack2(d1s0, d1s0), D1 = pack2(d1s1, d1s1), NM = pack2(-m1, -m1);
+                const uint4 o0 = dequant8x(qv[c].x, hh, D0, D1, NM);
+                const uint4 o1 = dequant8x(qv[c].y, hh, D0, D1, NM);
+                if (!mbar_wait(ba_empty + 8 * s, ((ks / SA) & 1) ^ 1, err)) { ok = false; break; }
                 // output chunk 4hh + 2p + v holds k = 32hh + 16p + 8v .. +7 of this 64-k step
                 uint8_t* arow = smem + Cfg::kOffA + s * kGemmAStageBytes + r * 128;
                 const int sw = r & 7;
-                const uint64_t D0 = pack2(d1s0, d1s0), D1 = pack2(d1s1, d1s1), NM = pack2(-m1, -m1);
-                *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p) ^ sw) << 4)) =
-                    dequant8x(q.x, hh, D0, D1, NM);
-                *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p + 1) ^ sw) << 4)) =
-                    dequant8x(q.y, hh, D0, D1, NM);
+                *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p) ^ sw) << 4)) = o0;
+                *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p + 1) ^ sw) << 4)) = o1;
                 fence_proxy_async_smem();
                 mbar_arrive(ba_full + 8 * s);
             }
-            mbar_arrive(bw_empty + 8 * ws);
         }
 
         // ------------------------------------------------- epilogue ---
