@@ -353,6 +353,64 @@ def run_profile_shape(args):
                       "device_error": q4k.q4k_device_error()}))
 
 
+def run_all_configs(args):
+    """Every workload of synth.WORKLOADS at every M and activation dtype it
+    names, each as full sweeps with q/k/v and gate/up grouped, in a CUDA graph;
+    one JSON line per case, plus the standalone dequant kernel."""
+    import torch
+    import gguf_q4_dequant_gb300 as q4k
+    from gguf_q4_dequant_gb300 import build as q4k_build
+    from gguf_q4_dequant_gb300 import synth
+    q4k_build.build()
+    torch.cuda.set_device(0)
+    q4k.q4k_init()
+    q4k.q4k_set_pdl(args.pdl)
+    dev = "cuda:0"
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    hbm, bf16_peak, _, _ = _peaks()
+    steps = max(3, min(args.steps, 20))
+    for wl in (1, 2, 3, 4):
+        w, mats, names = _weights(wl, dev, 0, with_names=True)
+        Ks = sorted({K for (_, _, K) in mats})
+        wbytes = sum(Wd.numel() for (Wd, _, _) in mats)
+        nk = sum(N * K for (_, N, K) in mats)
+        cases = [(M, x) for x in w.x_dtypes for M in w.decode_m]
+        cases += [(M, "bf16") for M in w.prefill_m]
+        for M, xdt in cases:
+            bf16 = xdt == "bf16"
+            dt = torch.bfloat16 if bf16 else torch.float32
+            xs = {K: synth.activations(synth.x_seed(wl, K, M), M, K, dt).to(dev) for K in Ks}
+            ny = sum(N for (_, N, _) in mats) if M == 1 else _group_y_floats(mats, names, M)
+            y = torch.empty(ny, device=dev)
+            calls = _grouped_calls(q4k, mats, names, xs, y, sp, M=M, bf16=bf16)
+            g = _capture(torch, calls, stream)
+            ms = _time_graph(torch, g, stream, steps, args.warmup, lambda: None)
+            gbps = wbytes / (ms * 1e-3) / 1e9
+            tf = 2 * M * nk / (ms * 1e-3) / 1e12
+            print(json.dumps({"workload": wl, "name": w.name, "M": M, "x_dtype": xdt,
+                              "kernel": "gemv_kernel" if M <= 16 else "gemm_kernel",
+                              "launches_per_sweep": len(calls), "steps": steps,
+                              "ms_per_sweep": round(ms, 4), "packed_GBps": round(gbps, 1),
+                              "frac_of_hbm": round(gbps / hbm, 4), "TFLOPs": round(tf, 2),
+                              "frac_of_bf16": round(tf / bf16_peak, 4),
+                              "device_error": q4k.q4k_device_error()}), flush=True)
+            del g, calls, xs, y
+        del mats
+        torch.cuda.empty_cache()
+    # K1: the lm_head of the Llama-3.2-3B shape expanded to fp32
+    N, K = 128256, 3072
+    Wd = synth.weight_rows(synth.weight_seed(2, 28, "lm_head"), N, K, device=dev)
+    out = torch.empty(N, K, device=dev)
+    g = _capture(torch, [lambda: q4k.q4k_dequant(Wd, N, K, out, stream=stream.cuda_stream)], stream)
+    ms = _time_graph(torch, g, stream, steps, args.warmup, lambda: None)
+    moved = Wd.numel() + out.numel() * 4
+    print(json.dumps({"kernel": "dequant_kernel", "shape": {"N": N, "K": K}, "ms": round(ms, 4),
+                      "read_plus_write_GBps": round(moved / (ms * 1e-3) / 1e9, 1),
+                      "frac_of_hbm": round(moved / (ms * 1e-3) / 1e9 / hbm, 4),
+                      "device_error": q4k.q4k_device_error()}), flush=True)
+
+
 def run_gpu(args):
     import torch
     import gguf_q4_dequant_gb300 as q4k
@@ -553,6 +611,8 @@ def main():
                     help="profiling aid: use only the first L layers of each weight set")
     ap.add_argument("--profile-shape", default="",
                     help="microbenchmark one shape 'N,K,M' (bf16 activations when M > 16)")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="time every workload at every M / X dtype (one JSON line each)")
     ap.add_argument("--profile-bytes", type=float, default=300e6,
                     help="weight bytes to rotate through in --profile-shape (> L2)")
     args = ap.parse_args()
@@ -562,6 +622,8 @@ def main():
         run_reference(args)
     elif args.profile_shape:
         run_profile_shape(args)
+    elif args.all_configs:
+        run_all_configs(args)
     else:
         run_gpu(args)
 

@@ -19,9 +19,10 @@
 //   CTA       = 4 consumer warps (warp w owns rows 32w..32w+31 of the tile,
 //               one lane per row and the whole super-block of that row per
 //               stage, so the per-stage and per-super-block set-up -- barrier
-//               waits, scale unpacking -- is paid once per 256 weights), 1 TMA
-//               producer warp and 1 activation warp. CTAs are persistent over
-//               tiles, so the stage ring streams continuously.
+//               waits, scale unpacking -- is paid once per 256 weights; for
+//               M >= 8 two such groups, each taking half of the activation
+//               rows), 1 TMA producer warp and 1 activation warp. CTAs are
+//               persistent over tiles, so the stage ring streams continuously.
 //
 // Per-weight arithmetic (the unpack happens in registers):
 //   A 4-bit quant q left in place inside its 32-bit word at bit 4p (p = 0..4)
@@ -48,7 +49,12 @@ constexpr int kGemvStageBytes = kGemvTileRows * kBlockBytes;  // 18432
 
 template <int MT>
 struct GemvCfg {
-    static constexpr int kConsumers = kGemvConsumers;
+    // M >= 8: two groups of consumer warps on the same rows and stages, each
+    // taking half of the activation rows (kML of them), so that a lane's
+    // accumulators fit and twice as many warps share the FMA work
+    static constexpr int kMGroups = MT >= 8 ? 2 : 1;
+    static constexpr int kML = MT / kMGroups;
+    static constexpr int kConsumers = kGemvConsumers * kMGroups;
     static constexpr int kProducerWarp = kConsumers;
     static constexpr int kStagerWarp = kConsumers + 1;
     static constexpr int kThreads = 32 * (kConsumers + 2);
@@ -184,9 +190,15 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
         const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c);
         const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(P + 32 + 32 * c);
         const uint64_t wp[4] = {qa.x, qa.y, qb.x, qb.y};
-        uint64_t lo_a[MT], lo_b[MT], hi_a[MT], hi_b[MT];  // fp32 pair accumulators
+        // fp32 pair accumulators: two independent chains per nibble half for
+        // small M; one for M >= 8, where the rows already give enough
+        // independent FMAs and the registers are needed
+        constexpr int NA = MT < 8 ? 2 : 1;
+        uint64_t lo[MT][NA], hi[MT][NA];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) lo_a[m] = lo_b[m] = hi_a[m] = hi_b[m] = 0ull;
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int a = 0; a < NA; ++a) lo[m][a] = hi[m][a] = 0ull;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const uint64_t Pw = wp[v];
@@ -203,20 +215,22 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
             for (int m = 0; m < MT; ++m) {
                 const ulonglong2* xp = reinterpret_cast<const ulonglong2*>(xs + m * 256 + 64 * c + 16 * v);
                 const ulonglong2 x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
-                lo_a[m] = fma2(qA, x0.x, lo_a[m]);
-                lo_b[m] = fma2(qC, x0.y, lo_b[m]);
-                lo_a[m] = fma2(qE, x1.x, lo_a[m]);
-                lo_b[m] = fma2(qG, x1.y, lo_b[m]);
-                hi_a[m] = fma2(qB, x2.x, hi_a[m]);
-                hi_b[m] = fma2(qD, x2.y, hi_b[m]);
-                hi_a[m] = fma2(qF, x3.x, hi_a[m]);
-                hi_b[m] = fma2(qH, x3.y, hi_b[m]);
+                lo[m][0] = fma2(qA, x0.x, lo[m][0]);
+                lo[m][NA - 1] = fma2(qC, x0.y, lo[m][NA - 1]);
+                lo[m][0] = fma2(qE, x1.x, lo[m][0]);
+                lo[m][NA - 1] = fma2(qG, x1.y, lo[m][NA - 1]);
+                hi[m][0] = fma2(qB, x2.x, hi[m][0]);
+                hi[m][NA - 1] = fma2(qD, x2.y, hi[m][NA - 1]);
+                hi[m][0] = fma2(qF, x3.x, hi[m][0]);
+                hi[m][NA - 1] = fma2(qH, x3.y, hi[m][NA - 1]);
             }
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            tot[m] = fma2(add2(lo_a[m], lo_b[m]), dsc[2 * c], tot[m]);
-            tot[m] = fma2(add2(hi_a[m], hi_b[m]), dsc[2 * c + 1], tot[m]);
+            const uint64_t L = NA == 2 ? add2(lo[m][0], lo[m][NA - 1]) : lo[m][0];
+            const uint64_t H = NA == 2 ? add2(hi[m][0], hi[m][NA - 1]) : hi[m][0];
+            tot[m] = fma2(L, dsc[2 * c], tot[m]);
+            tot[m] = fma2(H, dsc[2 * c + 1], tot[m]);
         }
     }
 #pragma unroll
@@ -268,7 +282,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             mbar_init(bar_empty + 8 * s, Cfg::kConsumers);  // every consumer warp reads every stage
         }
         // rank 0 of a cluster: one arrival per consumer warp of every other rank
-        mbar_init(bar_red, C > 1 ? (C - 1) * kGemvConsumers : 1);
+        mbar_init(bar_red, C > 1 ? (C - 1) * Cfg::kConsumers : 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -345,10 +359,12 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     } else {
         // ------------------------------------------------------- consumers ---
         pdl_wait();  // before any global write
-        const int r = 32 * warp + lane;  // row within the tile
-        float y[MT];
+        constexpr int ML = Cfg::kML;
+        const int r = 32 * (warp % kGemvConsumers) + lane;  // row within the tile
+        const int m0 = (warp / kGemvConsumers) * ML;        // first activation row of this warp
+        float y[ML];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) y[m] = 0.f;
+        for (int m = 0; m < ML; ++m) y[m] = 0.f;
         bool ok = true;  // after a timed-out wait the warp only keeps the barrier schedule
         for (int i = 0; i < nt_local; ++i) {
             for (int bl = 0; bl < nb; ++bl) {
@@ -356,14 +372,14 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 const int s = st % S;
                 ok = ok && mbar_wait(bar_full + 8 * s, (st / S) & 1, err);
                 if (ok) {
-                    float acc[MT];
+                    float acc[ML];
                     const uint8_t* P = smem + Cfg::kOffW + s * kGemvStageBytes + r * kBlockBytes;
-                    const float* xs = xs_ring + s * MT * 256;
-                    const float* xsm = xsum_ring + s * MT * 8;
-                    block_dot<MT>(P, xs, xsm, acc);
-                    const float* inv = inv_ring + s * MT * 2;
+                    const float* xs = xs_ring + (s * MT + m0) * 256;
+                    const float* xsm = xsum_ring + (s * MT + m0) * 8;
+                    block_dot<ML>(P, xs, xsm, acc);
+                    const float* inv = inv_ring + (s * MT + m0) * 2;
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
+                    for (int m = 0; m < ML; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * s);
@@ -375,8 +391,8 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 const int Nm = grp.N[mi];
                 float* Ym = grp.Y[mi];
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m < M && row < Nm) Ym[static_cast<int64_t>(m) * Nm + row] = y[m];
+                for (int m = 0; m < ML; ++m) {
+                    if (m0 + m < M && row < Nm) Ym[static_cast<int64_t>(m0 + m) * Nm + row] = y[m];
                     y[m] = 0.f;
                 }
             }
@@ -387,7 +403,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             if (rank != 0) {
                 const uint32_t dst = map_shared_rank(smem_u32(red + (rank - 1) * MT * kGemvTileRows), 0);
 #pragma unroll
-                for (int m = 0; m < MT; ++m) st_shared_cluster_f32(dst + 4 * (m * kGemvTileRows + r), y[m]);
+                for (int m = 0; m < ML; ++m) st_shared_cluster_f32(dst + 4 * ((m0 + m) * kGemvTileRows + r), y[m]);
                 // the warp's stores are ordered before lane 0's release-arrive
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(map_shared_rank(bar_red, 0));
@@ -397,10 +413,10 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 const int Nm = grp.N[mi];
                 float* Ym = grp.Y[mi];
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
+                for (int m = 0; m < ML; ++m) {
                     float v = y[m];
-                    for (int q = 1; q < C; ++q) v += red[(q - 1) * MT * kGemvTileRows + m * kGemvTileRows + r];
-                    if (m < M && row < Nm) Ym[static_cast<int64_t>(m) * Nm + row] = v;
+                    for (int q = 1; q < C; ++q) v += red[(q - 1) * MT * kGemvTileRows + (m0 + m) * kGemvTileRows + r];
+                    if (m0 + m < M && row < Nm) Ym[static_cast<int64_t>(m0 + m) * Nm + row] = v;
                 }
             }
             return;

@@ -26,3 +26,20 @@ def q4k():
     q4k_build.build()
     import gguf_q4_dequant_gb300 as lib
     return lib
+
+
+# worst |err| / tolerance per (workload, M, X dtype), filled by the full-size
+# parity tests and printed at the end of the run
+PARITY = {}
+
+
+@pytest.fixture(scope="session")
+def parity_record():
+    return PARITY
+
+
+def pytest_terminal_summary(terminalreporter):
+    if PARITY:
+        terminalreporter.write_line("worst |err| / tolerance over the sampled outputs, per (workload, M, X dtype):")
+        for k in sorted(PARITY):
+            terminalreporter.write_line(f"  workload {k[0]} M={k[1]} {k[2]}: {PARITY[k]:.4f}")
