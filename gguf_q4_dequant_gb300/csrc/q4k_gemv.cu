@@ -157,8 +157,8 @@ __device__ __forceinline__ void scale_activations(const float (&v)[8], int lane,
 
 // Rows kept in registers across one stage by the activation warp (the next
 // stage's loads are in flight while the current stage is written): all of
-// them for small M, none (load-and-use) for M >= 8 where the consumers are
-// compute-bound anyway.
+// them for small M; for M >= 8 the rows of a stage are loaded in batches of 8
+// whose loads are in flight together.
 template <int MT>
 struct XPrefetch {
     static constexpr int kRows = MT <= 4 ? MT : 0;
@@ -344,13 +344,23 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 for (int m = 0; m < PF; ++m)
                     scale_activations(cur[m], lane, xs + m * 256, xsum + m * 8, inv + 2 * m);
             } else {
-                if (!mbar_wait(bar_empty + 8 * s, ((st / S) & 1) ^ 1, err)) break;
+                // rows in batches of 8 whose loads are all in flight together
+                // (the first batch before the wait for the slot)
+                constexpr int B = MT < 8 ? MT : 8;
                 const int64_t kx = static_cast<int64_t>(kb0 + st % nb) * kBlockWeights + 8 * lane;
+                float v[B][8];
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    float v[8];
-                    load_x8<XB>(X, m, M, K, kx, v);
-                    scale_activations(v, lane, xs + m * 256, xsum + m * 8, inv + 2 * m);
+                for (int j = 0; j < B; ++j) load_x8<XB>(X, j, M, K, kx, v[j]);
+                if (!mbar_wait(bar_empty + 8 * s, ((st / S) & 1) ^ 1, err)) break;
+#pragma unroll
+                for (int m0 = 0; m0 < MT; m0 += B) {
+                    if (m0 > 0) {
+#pragma unroll
+                        for (int j = 0; j < B; ++j) load_x8<XB>(X, m0 + j, M, K, kx, v[j]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < B; ++j)
+                        scale_activations(v[j], lane, xs + (m0 + j) * 256, xsum + (m0 + j) * 8, inv + 2 * (m0 + j));
                 }
             }
             __syncwarp();
