@@ -310,6 +310,16 @@ __device__ __forceinline__ void cluster_wait() {
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
+// Asynchronous 4-byte store into another CTA's shared memory that counts its
+// bytes on that CTA's mbarrier `cluster_bar` (complete_tx); the issuing thread
+// does not wait for it.
+__device__ __forceinline__ void st_async_f32(uint32_t cluster_addr, float v, uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
+                     cluster_addr),
+                 "f"(v), "r"(cluster_bar)
+                 : "memory");
+}
+
 // Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

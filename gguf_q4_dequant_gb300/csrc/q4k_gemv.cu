@@ -10,9 +10,10 @@
 //               memory as [row][144] (a stage, 18 KB).
 //   K-slice   = a contiguous range of super-blocks. When there are fewer tiles
 //               than CTA slots, the K range is split across a thread-block
-//               cluster (one K-slice per CTA); ranks 1..C-1 store their partial
-//               sums into rank 0's shared memory and arrive on its mbarrier, and
-//               rank 0 adds them in rank order (deterministic).
+//               cluster (one K-slice per CTA); ranks 1..C-1 send their partial
+//               sums into rank 0's shared memory with st.async, which counts the
+//               bytes on rank 0's mbarrier, and rank 0 adds them in rank order
+//               (deterministic).
 //   group     = up to 8 weight matrices that share K and the activations (q, k
 //               and v of a layer; gate and up) are one launch: their tiles are
 //               numbered consecutively and each has its own TMA map and output.
@@ -281,9 +282,12 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             mbar_init(bar_full + 8 * s, 1 + 32);  // producer (with bytes) + 32 activation lanes
             mbar_init(bar_empty + 8 * s, Cfg::kConsumers);  // every consumer warp reads every stage
         }
-        // rank 0 of a cluster: one arrival per consumer warp of every other rank
-        mbar_init(bar_red, C > 1 ? (C - 1) * Cfg::kConsumers : 1);
+        // rank 0 of a cluster: the other ranks' partial sums land with
+        // st.async and count their bytes; rank 0's own arrival carries the total
+        mbar_init(bar_red, 1);
         fence_barrier_init();
+        if (C > 1 && rank == 0)
+            mbar_arrive_expect_tx(bar_red, (C - 1) * MT * kGemvTileRows * 4);
     }
     __syncthreads();
     if (C > 1) cluster_arrive_relaxed();  // the barriers above are ready for remote arrivals
@@ -413,10 +417,9 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             if (rank != 0) {
                 const uint32_t dst = map_shared_rank(smem_u32(red + (rank - 1) * MT * kGemvTileRows), 0);
 #pragma unroll
-                for (int m = 0; m < ML; ++m) st_shared_cluster_f32(dst + 4 * ((m0 + m) * kGemvTileRows + r), y[m]);
-                // the warp's stores are ordered before lane 0's release-arrive
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(map_shared_rank(bar_red, 0));
+                const uint32_t rbar = map_shared_rank(bar_red, 0);
+#pragma unroll
+                for (int m = 0; m < ML; ++m) st_async_f32(dst + 4 * ((m0 + m) * kGemvTileRows + r), y[m], rbar);
             } else if (mbar_wait(bar_red, 0, err)) {
                 const int mi = group_matrix(grp, cid);
                 const int row = (cid - grp.tile_start[mi]) * kGemvTileRows + r;
