@@ -373,6 +373,9 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     } else {
         // ------------------------------------------------------- consumers ---
         pdl_wait();  // before any global write
+        // every CTA of the cluster has initialised its barriers (waited for here,
+        // while the stage ring fills, rather than after the compute)
+        if (C > 1) cluster_wait();
         constexpr int ML = Cfg::kML;
         const int r = 32 * (warp % kGemvConsumers) + lane;  // row within the tile
         const int m0 = (warp / kGemvConsumers) * ML;        // first activation row of this warp
@@ -413,7 +416,6 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
         }
         if (C > 1) {
             // K-slices of this cluster's tile: ranks 1.. push into rank 0, which adds in rank order
-            cluster_wait();
             if (rank != 0) {
                 const uint32_t dst = map_shared_rank(smem_u32(red + (rank - 1) * MT * kGemvTileRows), 0);
 #pragma unroll
