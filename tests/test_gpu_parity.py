@@ -119,6 +119,20 @@ def test_gemv_ragged(q4k, oracle_mod, N, K, xdt):
         _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X, TOL_GEMV)
 
 
+@pytest.mark.parametrize("N", [1, 128, 300])
+@pytest.mark.parametrize("KB", [64, 37])
+@pytest.mark.parametrize("M,xdt", [(1, "f32"), (2, "f32"), (3, "bf16"), (16, "f32")])
+def test_gemv_split_k_widths(q4k, oracle_mod, N, KB, M, xdt):
+    """Few tiles and a long K: the launch splits K across clusters of up to 16
+    CTAs (8 for M > 2), with K-slices that do not divide K evenly (37 super-blocks);
+    the ranks' partial sums meet in rank 0's shared memory."""
+    K = 256 * KB
+    Wh = synth.weight_rows(7000 + N + KB, N, K)
+    dt = torch.bfloat16 if xdt == "bf16" else torch.float32
+    X = synth.activations(7100 + M + KB, M, K, dt)
+    _check_matmul(q4k, oracle_mod, Wh, Wh.to(DEV), N, K, X, TOL_GEMV)
+
+
 @pytest.mark.parametrize("M", [1, 4])
 def test_gemv_tiny_workload(q4k, oracle_mod, M):
     w = synth.WORKLOADS[0]
