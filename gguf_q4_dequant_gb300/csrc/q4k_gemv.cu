@@ -38,7 +38,8 @@
 //   weight give q*x*2^E with a single rounding and no int->float conversion.
 //   E is chosen from the block's largest |x| so that neither the scaled
 //   activations overflow nor the products leave the normal range. Sub-block
-//   sums are then combined as d*sc*S - dmin*m*sum(x) and scaled back by 2^-E.
+//   sums are then combined per super-block as d*sum(sc*S) - dmin*sum(m*sum(x))
+//   and scaled back by 2^-E.
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
 
@@ -172,17 +173,19 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
     const uint4 h = *reinterpret_cast<const uint4*>(P);
     const ScaleBytes sb = decode_scales(h.y, h.z, h.w);
     const float d = half_lo(h.x), dmin = half_hi(h.x);
-    uint64_t dsc[8];  // (d*sc_j, d*sc_j) pairs
-    float mm[8];      // dmin*m_j
+    // d and dmin are applied once per super-block, after the sums over its
+    // sub-blocks: d * sum_j sc_j*S_j - dmin * sum_j m_j*sum(x)_j
+    uint64_t scp[8];  // (sc_j, sc_j) pairs
+    float mf[8];      // m_j
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const uint32_t scw = j < 4 ? sb.sc_lo : sb.sc_hi;
         const uint32_t mw = j < 4 ? sb.m_lo : sb.m_hi;
-        const float a = d * byte_to_float(scw, j & 3);
-        dsc[j] = pack2(a, a);
-        mm[j] = dmin * byte_to_float(mw, j & 3);
+        const float a = byte_to_float(scw, j & 3);
+        scp[j] = pack2(a, a);
+        mf[j] = byte_to_float(mw, j & 3);
     }
-    uint64_t tot[MT];  // sum over sub-blocks of d*sc_j*S_j, as a pair
+    uint64_t tot[MT];  // sum over sub-blocks of sc_j*S_j, as a pair
 #pragma unroll
     for (int m = 0; m < MT; ++m) tot[m] = 0ull;
 #pragma unroll
@@ -230,8 +233,8 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
         for (int m = 0; m < MT; ++m) {
             const uint64_t L = NA == 2 ? add2(lo[m][0], lo[m][NA - 1]) : lo[m][0];
             const uint64_t H = NA == 2 ? add2(hi[m][0], hi[m][NA - 1]) : hi[m][0];
-            tot[m] = fma2(L, dsc[2 * c], tot[m]);
-            tot[m] = fma2(H, dsc[2 * c + 1], tot[m]);
+            tot[m] = fma2(L, scp[2 * c], tot[m]);
+            tot[m] = fma2(H, scp[2 * c + 1], tot[m]);
         }
     }
 #pragma unroll
@@ -239,9 +242,9 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
         const float* xsm = xsum + m * 8;
         float mins = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mins = fmaf(mm[j], xsm[j], mins);
+        for (int j = 0; j < 8; ++j) mins = fmaf(mf[j], xsm[j], mins);
         const float2 t = unpack2(tot[m]);
-        acc[m] = (t.x + t.y) - mins;
+        acc[m] = d * (t.x + t.y) - dmin * mins;
     }
 }
 
