@@ -126,6 +126,17 @@ def cpu_oracle_decode(budget_s: float, threads: int):
                       f"{elapsed:.1f} s of CPU time"}
 
 
+def max_over_ranks(times, ws, device="cpu"):
+    """Every timing as its maximum over the job's ranks (called by all ranks)."""
+    import torch
+    keys = sorted(times)
+    t = torch.tensor([times[k] for k in keys], device=device, dtype=torch.float64)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return dict(zip(keys, t.tolist()))
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -556,13 +567,7 @@ def run_gpu(args):
         out["_flops3"] = flops3
 
     out["clocks"] = sampler.stop()
-    # max over ranks
-    keys = sorted(times)
-    t = torch.tensor([times[k] for k in keys], device=dev, dtype=torch.float64)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    times = dict(zip(keys, t.tolist()))
+    times = max_over_ranks(times, ws, dev)
     out.pop("_names1", None) if "decode" not in times else None
     out["device_error"] = q4k.q4k_device_error()
     out["gpu_launches"] = launches
