@@ -93,17 +93,8 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 2-D tiled bulk tensor copy global -> shared, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                            int32_t y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Same with an L2 cache policy (createpolicy result).
+// 2-D tiled bulk tensor copy global -> shared, completing on `bar`, with an L2
+// cache policy (createpolicy result).
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int32_t x,
                                                  int32_t y, uint32_t bar, uint64_t policy) {
     asm volatile(
@@ -290,11 +281,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 
 // ------------------------------------------------------------ cluster ---
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
-    return r;
-}
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
@@ -320,22 +306,11 @@ __device__ __forceinline__ void st_async_f32(uint32_t cluster_addr, float v, uin
                  : "memory");
 }
 
-// Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
 // Address of the same shared variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
-}
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
 }
 
 // Programmatic dependent launch. Both are no-ops unless the kernel was launched
@@ -347,11 +322,6 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace q4k
