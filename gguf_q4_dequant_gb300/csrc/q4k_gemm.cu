@@ -42,20 +42,21 @@ constexpr int kGemmWStages = 3;  // a DRAM round trip is longer than one super-b
 constexpr int kGemmWStageBytes = kGemmBM * kBlockBytes;   // 18432
 constexpr int kGemmAStageBytes = kGemmBM * 128;           // 16384
 
-// Separate rings for the dequantised A tiles and the TMA-loaded X (B) tiles:
-// B is made as deep as shared memory allows, since its refill is an L2 round
-// trip issued only when the MMA of the slot's previous k-step completes.
+// One ring of k-steps, each holding a dequantised A tile and a TMA-loaded X
+// (B) tile, as deep as shared memory allows: a step's full barrier completes
+// when its X bytes have landed and every dequantising thread has arrived, and
+// one MMA commit releases both tiles, so the MMA-issuing warp waits once and
+// commits once per step.
 template <int BN>
 struct GemmCfg {
-    static constexpr int kAStages = BN == 256 ? 3 : 4;
-    static constexpr int kBStages = BN == 256 ? 3 : BN == 128 ? 5 : BN == 64 ? 6 : 8;
+    static constexpr int kStages = BN == 256 ? 3 : BN == 128 ? 5 : BN == 64 ? 6 : 8;
     static constexpr int kBStageBytes = BN * 128;
     static constexpr int kOffA = 0;                                            // 1024-aligned
-    static constexpr int kOffB = kOffA + kAStages * kGemmAStageBytes;          // 1024-aligned
-    static constexpr int kOffW = kOffB + kBStages * kBStageBytes;
+    static constexpr int kOffB = kOffA + kStages * kGemmAStageBytes;           // 1024-aligned
+    static constexpr int kOffW = kOffB + kStages * kBStageBytes;
     static constexpr int kOffBar = kOffW + kGemmWStages * kGemmWStageBytes;
-    // barriers: w_full[W], w_empty[W], a_full[SA], a_empty[SA], b_full[SB], b_empty[SB], acc_full
-    static constexpr int kNumBars = 2 * kGemmWStages + 2 * kAStages + 2 * kBStages + 1;
+    // barriers: w_full[W], w_empty[W], full[S], empty[S], acc_full
+    static constexpr int kNumBars = 2 * kGemmWStages + 2 * kStages + 1;
     static constexpr int kOffTmem = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffTmem + 16 + 1024;   // + alignment slack
     static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
@@ -97,8 +98,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ WeightGroup grp, const __grid_constant__ CUtensorMap tmapX,
                 int M, int K, int C, int kb_per, int pdl_flags, unsigned int* err) {
     using Cfg = GemmCfg<BN>;
-    constexpr int SA = Cfg::kAStages;
-    constexpr int SB = Cfg::kBStages;
+    constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -121,11 +121,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const uint32_t bw_full = sbase + Cfg::kOffBar;
     const uint32_t bw_empty = bw_full + 8 * kGemmWStages;
-    const uint32_t ba_full = bw_empty + 8 * kGemmWStages;
-    const uint32_t ba_empty = ba_full + 8 * SA;
-    const uint32_t bb_full = ba_empty + 8 * SA;
-    const uint32_t bb_empty = bb_full + 8 * SB;
-    const uint32_t bacc = bb_empty + 8 * SB;
+    const uint32_t bfull = bw_empty + 8 * kGemmWStages;
+    const uint32_t bempty = bfull + 8 * S;
+    const uint32_t bacc = bempty + 8 * S;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmem);
 
     if (threadIdx.x == 0) {
@@ -133,13 +131,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(bw_full + 8 * i, 1);
             mbar_init(bw_empty + 8 * i, kGemmDequantThreads);
         }
-        for (int i = 0; i < SA; ++i) {
-            mbar_init(ba_full + 8 * i, kGemmDequantThreads);
-            mbar_init(ba_empty + 8 * i, 1);
-        }
-        for (int i = 0; i < SB; ++i) {
-            mbar_init(bb_full + 8 * i, 1);
-            mbar_init(bb_empty + 8 * i, 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(bfull + 8 * i, kGemmDequantThreads + 1);  // + the producer's expect_tx arrival
+            mbar_init(bempty + 8 * i, 1);
         }
         mbar_init(bacc, 1);
         fence_barrier_init();
@@ -190,15 +184,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
                 if (ks < nks) {
-                    const int s = ks % SB;
-                    if (mbar_test_wait(bb_empty + 8 * s, ((ks / SB) & 1) ^ 1)) {
+                    const int s = ks % S;
+                    if (mbar_test_wait(bempty + 8 * s, ((ks / S) & 1) ^ 1)) {
                         if (!x_ready) {
                             pdl_wait();
                             x_ready = true;
                         }
-                        mbar_arrive_expect_tx(bb_full + 8 * s, Cfg::kBStageBytes);
+                        mbar_arrive_expect_tx(bfull + 8 * s, Cfg::kBStageBytes);
                         tma_load_2d_hint(sbase + Cfg::kOffB + s * Cfg::kBStageBytes, &tmapX,
-                                         (ks0 + ks) * kGemmKStep, m0, bb_full + 8 * s, pol_x);
+                                         (ks0 + ks) * kGemmKStep, m0, bfull + 8 * s, pol_x);
                         ++ks;
                         progress = true;
                     }
@@ -220,19 +214,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // descriptors stay warp-uniform); one elected lane issues.
         constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, BN);
         for (int ks = 0; ks < nks; ++ks) {
-            const int sa = ks % SA, sbs = ks % SB;
-            bool ok = mbar_wait(ba_full + 8 * sa, (ks / SA) & 1, err) &&
-                      mbar_wait(bb_full + 8 * sbs, (ks / SB) & 1, err);
+            const int s = ks % S;
+            const bool ok = mbar_wait(bfull + 8 * s, (ks / S) & 1, err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             if (elect_one()) {
-                const uint64_t a0 = sw128_desc(sbase + Cfg::kOffA + sa * kGemmAStageBytes);
-                const uint64_t b0 = sw128_desc(sbase + Cfg::kOffB + sbs * Cfg::kBStageBytes);
+                const uint64_t a0 = sw128_desc(sbase + Cfg::kOffA + s * kGemmAStageBytes);
+                const uint64_t b0 = sw128_desc(sbase + Cfg::kOffB + s * Cfg::kBStageBytes);
 #pragma unroll
                 for (int kk = 0; kk < kGemmKStep / 16; ++kk)  // +32 bytes per k16 = +2 in the address field
                     tc_mma_bf16(tmem, a0 + 2 * kk, b0 + 2 * kk, idesc, (ks | kk) != 0);
-                tc_commit(ba_empty + 8 * sa);
-                tc_commit(bb_empty + 8 * sbs);
+                tc_commit(bempty + 8 * s);
             }
             __syncwarp();
         }
@@ -263,7 +255,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int ks = sb * 4 + c;
-                const int s = ks % SA;
+                const int s = ks % S;
                 const int j = 2 * c + hh;  // sub-block
                 const uint32_t scw = j < 4 ? scb.sc_lo : scb.sc_hi;
                 const uint32_t mw = j < 4 ? scb.m_lo : scb.m_hi;
@@ -273,14 +265,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint64_t D0 = pack2(d1s0, d1s0), D1 = pack2(d1s1, d1s1), NM = pack2(-m1, -m1);
                 const uint4 o0 = dequant8x(qv[c].x, hh, D0, D1, NM);
                 const uint4 o1 = dequant8x(qv[c].y, hh, D0, D1, NM);
-                if (!mbar_wait(ba_empty + 8 * s, ((ks / SA) & 1) ^ 1, err)) { ok = false; break; }
+                if (!mbar_wait(bempty + 8 * s, ((ks / S) & 1) ^ 1, err)) { ok = false; break; }
                 // output chunk 4hh + 2p + v holds k = 32hh + 16p + 8v .. +7 of this 64-k step
                 uint8_t* arow = smem + Cfg::kOffA + s * kGemmAStageBytes + r * 128;
                 const int sw = r & 7;
                 *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p) ^ sw) << 4)) = o0;
                 *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p + 1) ^ sw) << 4)) = o1;
                 fence_proxy_async_smem();
-                mbar_arrive(ba_full + 8 * s);
+                mbar_arrive(bfull + 8 * s);
             }
         }
 
