@@ -25,7 +25,8 @@ Q4K_ERR_TIMEOUT = -6
 
 #: every symbol include/q4k.h declares
 EXPORTS = ("q4k_status_string", "q4k_init", "q4k_dequant", "q4k_matmul", "q4k_matmul_bf16",
-           "q4k_matmul_multi", "q4k_matmul_multi_bf16", "q4k_set_pdl", "q4k_device_error")
+           "q4k_matmul_multi", "q4k_matmul_multi_bf16", "q4k_matmul_argmax",
+           "q4k_matmul_argmax_bf16", "q4k_set_pdl", "q4k_device_error")
 MAX_GROUP = 8
 
 
@@ -70,6 +71,10 @@ def lib() -> ctypes.CDLL:
             L.q4k_matmul_multi.restype = ctypes.c_int
             L.q4k_matmul_multi_bf16.argtypes = [ctypes.c_int, vpp, i64p, i64, vp, i64, vpp, vp]
             L.q4k_matmul_multi_bf16.restype = ctypes.c_int
+            L.q4k_matmul_argmax.argtypes = [vp, i64, i64, vp, i64, vp, vp]
+            L.q4k_matmul_argmax.restype = ctypes.c_int
+            L.q4k_matmul_argmax_bf16.argtypes = [vp, i64, i64, vp, i64, vp, vp]
+            L.q4k_matmul_argmax_bf16.restype = ctypes.c_int
             L.q4k_set_pdl.argtypes = [ctypes.c_int]
             L.q4k_set_pdl.restype = ctypes.c_int
             L.q4k_device_error.argtypes = [ctypes.c_int]
@@ -161,6 +166,28 @@ def q4k_matmul_multi(Ws, Ns, K: int, X, M: int, Ys, stream=None):
     y_arr = (ctypes.c_void_p * count)(*[_ptr(Y) for Y in Ys])
     fn = lib().q4k_matmul_multi_bf16 if bf16 else lib().q4k_matmul_multi
     _check(fn(count, w_arr, n_arr, K, _ptr(X), M, y_arr, _stream(stream)), "q4k_matmul_multi")
+
+
+def q4k_matmul_argmax(W, N: int, K: int, X, M: int, out, stream=None):
+    """out[m] = argmax_n (X[M, K] * W^T)[m, n] (int64, lowest n on ties), fp32 or bf16 X, M <= 16."""
+    import torch
+    _check_dtype(W, torch.uint8, "W")
+    _check_dtype(out, torch.int64, "out")
+    bf16 = not isinstance(X, int) and X.dtype == torch.bfloat16
+    if not bf16:
+        _check_dtype(X, torch.float32, "X")
+    fn = lib().q4k_matmul_argmax_bf16 if bf16 else lib().q4k_matmul_argmax
+    _check(fn(_ptr(W), N, K, _ptr(X), M, _ptr(out), _stream(stream)), "q4k_matmul_argmax")
+
+
+def argmax(W, N: int, K: int, X, out=None, stream=None):
+    """Convenience: the fused argmax, allocating out with torch if not given."""
+    import torch
+    M = X.shape[0]
+    if out is None:
+        out = torch.empty(M, dtype=torch.int64, device=X.device)
+    q4k_matmul_argmax(W, N, K, X, M, out, stream)
+    return out
 
 
 def q4k_set_pdl(mode: int) -> int:

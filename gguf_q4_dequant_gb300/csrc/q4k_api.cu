@@ -10,6 +10,7 @@
 //                   M >= 17  -> K3 gemm_kernel (tcgen05, TMEM accumulators)
 //   q4k_matmul_multi[_bf16]  -> the same, for up to 8 matrices sharing K and X,
 //                   all of them in one launch (per 16-row slice for fp32 M > 16)
+//   q4k_matmul_argmax[_bf16] -> K2 with the fused argmax epilogue (M <= 16)
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -176,6 +177,33 @@ int run_gemm(int count, const void* const* W, const int64_t* N, int64_t K, const
     return Q4K_OK;
 }
 
+// Fused GEMV + argmax (M <= 16): the keys live in `out` itself until the last
+// kernel turns them into row indices.
+int run_argmax(const void* W, int64_t N, int64_t K, const void* X, bool xb, int64_t M, int64_t* out,
+               cudaStream_t stream, const DeviceInfo& dev) {
+    WeightGroup grp;
+    const int rc = make_group(&grp, 1, &W, &N, K);
+    if (rc != Q4K_OK) return rc;
+    grp.Y[0] = nullptr;
+    auto* keys = reinterpret_cast<unsigned long long*>(out);
+    const int m = static_cast<int>(M);
+    if (launch_argmax_init(keys, m, stream) != cudaSuccess ||
+        launch_gemv(grp, X, xb, m, static_cast<int>(K), stream, dev,
+                    g_pdl.load(std::memory_order_relaxed), keys) != cudaSuccess ||
+        launch_argmax_finish(keys, m, stream) != cudaSuccess)
+        return Q4K_ERR_CUDA;
+    return Q4K_OK;
+}
+
+int check_argmax(const void* W, int64_t N, int64_t K, const void* X, int64_t M, const int64_t* out) {
+    if (!W || !X || !out) return Q4K_ERR_NULL;
+    const int rc = check_dims(N, K);
+    if (rc != Q4K_OK) return rc;
+    if (M < 1 || M > 16) return Q4K_ERR_BAD_DIM;
+    if (!aligned16(W) || !aligned16(X) || (reinterpret_cast<uintptr_t>(out) & 7u) != 0) return Q4K_ERR_ALIGN;
+    return Q4K_OK;
+}
+
 // Checks shared by the single and grouped matmul calls.
 int check_matmul(int count, const void* const* W, const int64_t* N, int64_t K, const void* X,
                  int64_t M, float* const* Y) {
@@ -271,6 +299,24 @@ int q4k_matmul_multi_bf16(int count, const void* const* W, const int64_t* N, int
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M <= 16) return run_gemv(count, W, N, K, X_bf16, true, M, Y, st, *dev);
     return run_gemm(count, W, N, K, X_bf16, M, Y, st, *dev);
+}
+
+int q4k_matmul_argmax(const void* W, int64_t N, int64_t K, const float* X, int64_t M,
+                      int64_t* out_idx, void* stream) {
+    int rc = check_argmax(W, N, K, X, M, out_idx);
+    if (rc != Q4K_OK) return rc;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = current_device(&dev)) != Q4K_OK) return rc;
+    return run_argmax(W, N, K, X, false, M, out_idx, static_cast<cudaStream_t>(stream), *dev);
+}
+
+int q4k_matmul_argmax_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16, int64_t M,
+                           int64_t* out_idx, void* stream) {
+    int rc = check_argmax(W, N, K, X_bf16, M, out_idx);
+    if (rc != Q4K_OK) return rc;
+    const DeviceInfo* dev = nullptr;
+    if ((rc = current_device(&dev)) != Q4K_OK) return rc;
+    return run_argmax(W, N, K, X_bf16, true, M, out_idx, static_cast<cudaStream_t>(stream), *dev);
 }
 
 int q4k_set_pdl(int mode) {

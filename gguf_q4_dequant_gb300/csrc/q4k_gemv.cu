@@ -252,10 +252,33 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
 // shares tiles and splits K into C slices of kb_per super-blocks. With C > 1
 // every cluster owns exactly one tile.
 
+// Argmax of a row of Y (fused lm_head + greedy pick): a 64-bit key that orders
+// (logit, row) pairs by larger logit first, then lower row index; NaN ranks
+// below every number. The high word is the logit's bit pattern made
+// order-preserving as an unsigned integer, the low word the row's complement.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
+    const uint32_t u = __float_as_uint(v);
+    uint32_t hi = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    if (v != v) hi = 0u;
+    return (static_cast<unsigned long long>(hi) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(n));
+}
+
+// The warp's largest key, combined into keys[m] (the maximum does not depend on
+// the order in which warps arrive, so the result is deterministic).
+__device__ __forceinline__ void argmax_combine(unsigned long long key, int lane, bool valid_m,
+                                               unsigned long long* keys_m) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long t = __shfl_xor_sync(0xffffffffu, key, o);
+        key = t > key ? t : key;
+    }
+    if (lane == 0 && valid_m) atomicMax(keys_m, key);
+}
+
 template <int MT, bool XB>
 __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks)
     gemv_kernel(const __grid_constant__ WeightGroup grp, const void* __restrict__ X, int M, int K,
-                int C, int kb_per, int pdl_flags, unsigned int* err) {
+                int C, int kb_per, int pdl_flags, unsigned long long* amax, unsigned int* err) {
     using Cfg = GemvCfg<MT>;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -412,7 +435,11 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 float* Ym = grp.Y[mi];
 #pragma unroll
                 for (int m = 0; m < ML; ++m) {
-                    if (m0 + m < M && row < Nm) Ym[static_cast<int64_t>(m0 + m) * Nm + row] = y[m];
+                    if (amax != nullptr)
+                        argmax_combine(row < Nm ? argmax_key(y[m], row) : 0ull, lane, m0 + m < M,
+                                       amax + m0 + m);
+                    else if (m0 + m < M && row < Nm)
+                        Ym[static_cast<int64_t>(m0 + m) * Nm + row] = y[m];
                     y[m] = 0.f;
                 }
             }
@@ -425,7 +452,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 const uint32_t rbar = map_shared_rank(bar_red, 0);
 #pragma unroll
                 for (int m = 0; m < ML; ++m) st_async_f32(dst + 4 * ((m0 + m) * kGemvTileRows + r), y[m], rbar);
-            } else if (mbar_wait(bar_red, 0, err)) {
+            } else if (__all_sync(0xffffffffu, mbar_wait(bar_red, 0, err))) {  // warp-uniform (argmax shuffles)
                 const int mi = group_matrix(grp, cid);
                 const int row = (cid - grp.tile_start[mi]) * kGemvTileRows + r;
                 const int Nm = grp.N[mi];
@@ -434,7 +461,11 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 for (int m = 0; m < ML; ++m) {
                     float v = y[m];
                     for (int q = 1; q < C; ++q) v += red[(q - 1) * MT * kGemvTileRows + (m0 + m) * kGemvTileRows + r];
-                    if (m0 + m < M && row < Nm) Ym[static_cast<int64_t>(m0 + m) * Nm + row] = v;
+                    if (amax != nullptr)
+                        argmax_combine(row < Nm ? argmax_key(v, row) : 0ull, lane, m0 + m < M,
+                                       amax + m0 + m);
+                    else if (m0 + m < M && row < Nm)
+                        Ym[static_cast<int64_t>(m0 + m) * Nm + row] = v;
                 }
             }
             return;
@@ -500,7 +531,7 @@ cudaError_t gemv_setup() {
 
 template <int MT, bool XB>
 static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K, cudaStream_t stream,
-                             const DeviceInfo& dev, int slot, int pdl) {
+                             const DeviceInfo& dev, int slot, int pdl, unsigned long long* amax) {
     const int KB = K / kBlockWeights;
     const int tiles = grp.tile_start[grp.count];
     const int slots = dev.num_sms * g_occ[XB ? 1 : 0][slot];
@@ -553,21 +584,39 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
     // pdl_flags bit 0: the producer also waits for the preceding grid before
     // streaming W (cleared only when the caller allows weight prefetch).
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, XB>, grp, X, M, K, C, kb_per, pdl_flags, dev.err);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, XB>, grp, X, M, K, C, kb_per, pdl_flags, amax,
+                              dev.err);
 }
 
 cudaError_t launch_gemv(const WeightGroup& grp, const void* X, bool x_bf16, int M, int K,
-                        cudaStream_t stream, const DeviceInfo& dev, int pdl) {
+                        cudaStream_t stream, const DeviceInfo& dev, int pdl, unsigned long long* amax) {
     const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
 #define Q4K_CASE(MT, SLOT)                                                            \
     case MT:                                                                          \
-        return x_bf16 ? launch_mt<MT, true>(grp, X, M, K, stream, dev, SLOT, pdl)     \
-                      : launch_mt<MT, false>(grp, X, M, K, stream, dev, SLOT, pdl);
+        return x_bf16 ? launch_mt<MT, true>(grp, X, M, K, stream, dev, SLOT, pdl, amax)   \
+                      : launch_mt<MT, false>(grp, X, M, K, stream, dev, SLOT, pdl, amax);
     switch (mt) {
         Q4K_CASE(1, 0) Q4K_CASE(2, 1) Q4K_CASE(4, 2) Q4K_CASE(8, 3) Q4K_CASE(16, 4)
     }
 #undef Q4K_CASE
     return cudaErrorInvalidValue;
+}
+
+// Keys of the fused argmax: cleared before the GEMV, turned into row indices after it.
+__global__ void argmax_init_kernel(unsigned long long* keys, int M) {
+    if (static_cast<int>(threadIdx.x) < M) keys[threadIdx.x] = 0ull;
+}
+__global__ void argmax_finish_kernel(unsigned long long* keys, int M) {
+    if (static_cast<int>(threadIdx.x) < M) keys[threadIdx.x] = 0xFFFFFFFFull - (keys[threadIdx.x] & 0xFFFFFFFFull);
+}
+
+cudaError_t launch_argmax_init(unsigned long long* keys, int M, cudaStream_t stream) {
+    argmax_init_kernel<<<1, 32, 0, stream>>>(keys, M);
+    return cudaGetLastError();
+}
+cudaError_t launch_argmax_finish(unsigned long long* keys, int M, cudaStream_t stream) {
+    argmax_finish_kernel<<<1, 32, 0, stream>>>(keys, M);
+    return cudaGetLastError();
 }
 
 }  // namespace q4k

@@ -43,8 +43,13 @@ __host__ __device__ inline int group_matrix(const WeightGroup& g, int t) {
     while (i + 1 < g.count && t >= g.tile_start[i + 1]) ++i;
     return i;
 }
+// amax != nullptr: no Y is written; the argmax key of each activation row's
+// outputs (see argmax_key) is combined into amax[m] instead (count == 1).
 cudaError_t launch_gemv(const WeightGroup& grp, const void* X, bool x_bf16, int M, int K,
-                        cudaStream_t stream, const DeviceInfo& dev, int pdl);
+                        cudaStream_t stream, const DeviceInfo& dev, int pdl,
+                        unsigned long long* amax = nullptr);
+cudaError_t launch_argmax_init(unsigned long long* keys, int M, cudaStream_t stream);
+cudaError_t launch_argmax_finish(unsigned long long* keys, int M, cudaStream_t stream);
 cudaError_t gemv_setup();
 
 // tcgen05 GEMM for M >= 17 rows of bf16 activations over a group of weight

@@ -113,6 +113,23 @@ int q4k_matmul_multi_bf16(int count, const void* const* W, const int64_t* N, int
                           const uint16_t* X_bf16, int64_t M, float* const* Y, void* stream);
 
 /*
+ * Fused lm_head + greedy pick (the device-side version of the host-greedy
+ * decode of the "rlx-llama32" crate page, section "Env flags"; the in-graph
+ * lm_head there is a DequantMatMul like every other matmul): out_idx[m] =
+ * argmax_n Y[m][n] for Y = X * W^T, for 1 <= M <= 16 rows of activations,
+ * without writing Y. Ties go to the lowest n; NaN outputs are never picked
+ * unless every output of the row is NaN (then 0). Y itself is computed as by
+ * q4k_matmul / q4k_matmul_bf16 (accuracy 1e-4 * sum|X*w|), so rows whose two
+ * largest outputs differ by less than that may pick either. out_idx: device,
+ * int64 [M], 8-byte aligned; it is overwritten (it holds intermediate keys
+ * while the call runs). Three kernels on `stream`; allocates nothing.
+ */
+int q4k_matmul_argmax(const void* W, int64_t N, int64_t K, const float* X, int64_t M,
+                      int64_t* out_idx, void* stream);
+int q4k_matmul_argmax_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16, int64_t M,
+                           int64_t* out_idx, void* stream);
+
+/*
  * Programmatic dependent launch for every later call in the process (a
  * decode step issues one call per weight matrix, so the gaps between
  * back-to-back kernels matter). Returns the previous mode, or

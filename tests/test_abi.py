@@ -118,3 +118,16 @@ def test_grouped_call_host_checks(q4k):
     Ym = (C.c_void_p * 3)(A16, A16 + 4, A16)
     assert L.q4k_matmul_multi(3, W, N, 256, A16, 1, Ym, None) == q4k.Q4K_ERR_ALIGN
     assert L.q4k_matmul_multi(3, W, N, 300, A16, 1, Y, None) == q4k.Q4K_ERR_BAD_DIM
+
+
+def test_argmax_host_checks(q4k):
+    L = q4k.lib()
+    for f in (L.q4k_matmul_argmax, L.q4k_matmul_argmax_bf16):
+        assert f(None, 4, 256, A16, 1, A16, None) == q4k.Q4K_ERR_NULL
+        assert f(A16, 4, 256, None, 1, A16, None) == q4k.Q4K_ERR_NULL
+        assert f(A16, 4, 256, A16, 1, None, None) == q4k.Q4K_ERR_NULL
+        assert f(A16, 4, 256, A16, 0, A16, None) == q4k.Q4K_ERR_BAD_DIM
+        assert f(A16, 4, 256, A16, 17, A16, None) == q4k.Q4K_ERR_BAD_DIM   # decode only
+        assert f(A16, 4, 300, A16, 1, A16, None) == q4k.Q4K_ERR_BAD_DIM
+        assert f(A16, 4, 256, A16, 1, A16 + 4, None) == q4k.Q4K_ERR_ALIGN  # int64 out: 8-byte aligned
+        assert f(A16, 4, 256, A16 + 8, 1, A16, None) == q4k.Q4K_ERR_ALIGN

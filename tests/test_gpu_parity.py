@@ -403,3 +403,93 @@ def test_grouped_matmul_in_graph_with_pdl(q4k):
             assert torch.allclose(a, r, rtol=0, atol=1e-3)
     finally:
         q4k.q4k_set_pdl(old)
+
+
+# ---------------------------------------------------------- fused argmax ---
+
+def _argmax_valid(oracle_mod, Wh, N, K, X, got):
+    """got[m] is a correct argmax of row m under the oracle: within the GEMV
+    bar of the exact maximum (rows whose leaders differ by less than that may
+    pick either)."""
+    Yref, A = oracle_mod.matmul(Wh.numpy(), N, K, _x_for_oracle(oracle_mod, X))
+    for m, n in enumerate(got):
+        best = int(np.argmax(Yref[m]))
+        slack = TOL_GEMV * (A[m, n] + A[m, best])
+        assert Yref[m, n] >= Yref[m, best] - slack, (m, n, best)
+
+
+@pytest.mark.parametrize("N,K", [(300, 512), (1000, 2048), (4097, 768)])
+@pytest.mark.parametrize("M,xdt", [(1, "f32"), (4, "bf16"), (16, "f32")])
+def test_argmax_matches_gemv_and_oracle(q4k, oracle_mod, N, K, M, xdt):
+    """The fused argmax equals the argmax (first maximum) of the library's own
+    GEMV outputs -- the same kernel computes the same values -- and is a correct
+    argmax of the exact product."""
+    Wh = synth.weight_rows(9000 + N + K, N, K)
+    Wd = Wh.to(DEV)
+    dt = torch.bfloat16 if xdt == "bf16" else torch.float32
+    X = synth.activations(9100 + M, M, K, dt)
+    Xd = X.to(DEV)
+    out = torch.full((M,), -7, dtype=torch.int64, device=DEV)
+    q4k.q4k_matmul_argmax(Wd, N, K, Xd, M, out)
+    Y = q4k.matmul(Wd, N, K, Xd)
+    torch.cuda.synchronize()
+    got = out.cpu().tolist()
+    assert got == torch.argmax(Y, dim=1).cpu().tolist()
+    _argmax_valid(oracle_mod, Wh, N, K, X, got)
+
+
+def test_argmax_ties_go_to_the_lowest_index(q4k):
+    """Rows with identical bytes give identical outputs; when they hold the
+    maximum, the lowest of them is returned."""
+    N, K, M = 2000, 1024, 3
+    W = synth.weight_rows(9200, N, K)
+    X = synth.activations(9201, M, K).to(DEV)
+    Wd = W.to(DEV)
+    first = q4k.argmax(Wd, N, K, X).cpu().tolist()
+    for m in range(M):
+        top = first[m]
+        W2 = W.clone()
+        for dst in (top // 3, top // 3 + 1, N - 1):  # copies below and above it
+            W2[dst] = W[top]
+        got = q4k.argmax(W2.to(DEV), N, K, X).cpu().tolist()
+        assert got[m] == min(top // 3, top), (m, got[m], top)
+
+
+def test_argmax_lm_head_full_size(q4k, oracle_mod):
+    """The tied lm_head of the Llama-3.2-3B shape (128256 x 3072), M = 1, at full
+    size: equal to the GEMV's argmax and valid under the oracle."""
+    N, K = 128256, 3072
+    seed = synth.weight_seed(2, 28, "lm_head")
+    Wd = synth.weight_rows(seed, N, K, device=DEV)
+    X = synth.activations(synth.x_seed(2, K, 1), 1, K)
+    Xd = X.to(DEV)
+    got = q4k.argmax(Wd, N, K, Xd).cpu().tolist()
+    Y = q4k.matmul(Wd, N, K, Xd)
+    assert got == torch.argmax(Y, dim=1).cpu().tolist()
+    Wh = Wd.cpu()
+    del Wd
+    torch.cuda.empty_cache()
+    _argmax_valid(oracle_mod, Wh, N, K, X, got)
+
+
+def test_argmax_in_graph_with_pdl(q4k):
+    N, K = 5000, 2048
+    Wd = synth.weight_rows(9300, N, K).to(DEV)
+    X = synth.activations(9301, 2, K).to(DEV)
+    ref = q4k.argmax(Wd, N, K, X).clone()
+    old = q4k.q4k_set_pdl(2)
+    try:
+        s = torch.cuda.Stream()
+        out = torch.full((2,), -1, dtype=torch.int64, device=DEV)
+        with torch.cuda.stream(s):
+            q4k.q4k_matmul_argmax(Wd, N, K, X, 2, out)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                q4k.q4k_matmul_argmax(Wd, N, K, X, 2, out)
+            out.fill_(-1)
+            g.replay()
+            s.synchronize()
+        assert torch.equal(out, ref)
+    finally:
+        q4k.q4k_set_pdl(old)
