@@ -527,6 +527,40 @@ def run_gpu(args):
         del mats1, calls1
         torch.cuda.empty_cache()
 
+        # the lm_head of the Llama-3.2-3B shape as a greedy pick: the fused
+        # GEMV + argmax call against the GEMV followed by torch's argmax
+        import ctypes
+        lib = q4k.lib()
+        Nl, Kl = 128256, 3072
+        Wl = synth.weight_rows(synth.weight_seed(2, 28, "lm_head"), Nl, Kl, device=dev)
+        xl = synth.activations(synth.x_seed(2, Kl, 1), 1, Kl).to(dev)
+        yl = torch.empty(1, Nl, device=dev)
+        idx = torch.empty(1, dtype=torch.int64, device=dev)
+        idx2 = torch.empty(1, dtype=torch.int64, device=dev)
+
+        def fused():
+            rc = lib.q4k_matmul_argmax(Wl.data_ptr(), Nl, Kl, xl.data_ptr(), 1, idx.data_ptr(), sp)
+            if rc != 0:
+                raise q4k.Q4KError(rc, "lm_head argmax")
+
+        def two_step():
+            rc = lib.q4k_matmul(Wl.data_ptr(), Nl, Kl, xl.data_ptr(), 1, yl.data_ptr(), sp)
+            if rc != 0:
+                raise q4k.Q4KError(rc, "lm_head gemv")
+            torch.argmax(yl, dim=1, out=idx2)
+        gf = _capture(torch, [fused], stream)
+        times["lm_head_argmax"] = _time_graph(torch, gf, stream, args.steps, args.warmup, barrier)
+        launches += args.steps * 3
+        gt = _capture(torch, [two_step], stream)
+        times["lm_head_gemv_then_argmax"] = _time_graph(torch, gt, stream, args.steps, args.warmup, barrier)
+        launches += args.steps
+        torch.cuda.synchronize()
+        if not torch.equal(idx, idx2):
+            raise RuntimeError("fused argmax differs from the GEMV's argmax")
+        out["_lm_head_bytes"] = Wl.numel()
+        del gf, gt, Wl
+        torch.cuda.empty_cache()
+
     if args.only in ("all", "prefill"):
         w3, mats3, names3 = _weights(PREFILL_WL, dev, args.layers, with_names=True)
         Ks = sorted({K for (_, _, K) in mats3})
@@ -583,6 +617,13 @@ def run_gpu(args):
             "launches_per_step": len(out.pop("_names1"))}
         out["e2e"]["value"] = round(ws * b1 / (times["e2e"] * 1e-3) / 1e9, 2)
         out["e2e"]["ms_per_step"] = round(times["e2e"], 4)
+        lb = out.pop("_lm_head_bytes")
+        out["lm_head_argmax"] = {
+            "workload": "lm_head 128256 x 3072 (Llama-3.2-3B shape), M=1 fp32, greedy pick",
+            "fused_us": round(times["lm_head_argmax"] * 1e3, 2),
+            "fused_packed_GBps": round(lb / (times["lm_head_argmax"] * 1e-3) / 1e9, 1),
+            "gemv_then_torch_argmax_us": round(times["lm_head_gemv_then_argmax"] * 1e3, 2),
+            "same_index": True}
     if "prefill" in times:
         f3 = out.pop("_flops3")
         out["gemm"]["value"] = round(ws * f3 / (times["prefill"] * 1e-3) / 1e12, 2)
