@@ -11,22 +11,25 @@
 //   accumulator    = 128 TMEM lanes x BN fp32 columns
 // so each dequantised weight tile is reused across all BN tokens of the tile.
 //
-// Warp roles (320 threads):
+// Warp roles (576 threads, one CTA per SM):
 //   warp 0      TMA producer: packed W super-block tiles {144 B, 128 rows}
-//               and X tiles {64 k, BN rows} (128-byte swizzle), two rings
-//               refilled independently
-//   warp 1      TMEM allocator and MMA issuer (one elected thread)
+//               (their own ring) and X tiles {64 k, BN rows} (128-byte
+//               swizzle, into the k-step ring); both rings refilled as soon as
+//               a slot frees
+//   warp 1      TMEM allocator and MMA issuer (the warp runs the loop, one
+//               elected lane issues: 4 MMAs of K = 16 and one commit per step)
 //   warps 2..17 dequantisers (thread t <-> weight row t % 128; t / 128 picks
 //               the nibble half and which 16 of the chunk's 32 qs bytes): read
-//               the packed block from shared memory and write 16 bf16 weights
+//               a super-block's bytes into registers and write 16 bf16 weights
 //               per k-step into the swizzled A tile; then the epilogue (TMEM ->
 //               registers -> Y, 128-byte coalesced stores per token column;
 //               four warps per TMEM lane quadrant).
 // When the tiles alone cannot fill the GPU, K is split across a thread-block
 // cluster of C CTAs: each CTA pushes the accumulator rows owned by rank r
-// (rows [r*ceil(128/C), ...)) from TMEM into rank r's shared memory through
-// distributed shared memory, and rank r adds the C partials in rank order
-// (deterministic).
+// (rows [r*rows, (r+1)*rows), rows = ceil(128/C) rounded up to a multiple of 4)
+// from TMEM into rank r's shared memory through distributed shared memory, and
+// rank r adds the C partials in rank order (deterministic). Several matrices
+// sharing K and X run as one launch (global tile -> matrix, as for the GEMV).
 // All pipeline waits are bounded (see mbar_wait).
 #include "q4k_device.cuh"
 #include "q4k_internal.h"

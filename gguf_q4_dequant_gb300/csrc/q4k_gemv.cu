@@ -40,6 +40,10 @@
 //   activations overflow nor the products leave the normal range. Sub-block
 //   sums are then combined per super-block as d*sum(sc*S) - dmin*sum(m*sum(x))
 //   and scaled back by 2^-E.
+//
+// Epilogue: one store per lane and activation row, or, for the fused greedy
+// pick (q4k_matmul_argmax), a warp-wide maximum of 64-bit (logit, row) keys
+// combined into the caller's output with atomicMax -- no Y is written.
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
 
@@ -61,7 +65,8 @@ struct GemvCfg {
     static constexpr int kStagerWarp = kConsumers + 1;
     static constexpr int kThreads = 32 * (kConsumers + 2);
     // registers: two resident CTAs per SM for small M (measured: more registers
-    // per thread buy more overlap than a third CTA would); M >= 8 needs ~250
+    // per thread buy more overlap than a third CTA would); M >= 8 takes ~145-165
+    // registers a thread at 320 threads, one CTA per SM
     static constexpr int kMinBlocks = MT >= 8 ? 1 : 2;
     static constexpr int kStages = 4;
     static constexpr int kOffW = 0;
@@ -248,10 +253,6 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
     }
 }
 
-// Grid: gridDim.x = (number of clusters) * C; a cluster of C CTAs along x
-// shares tiles and splits K into C slices of kb_per super-blocks. With C > 1
-// every cluster owns exactly one tile.
-
 // Argmax of a row of Y (fused lm_head + greedy pick): a 64-bit key that orders
 // (logit, row) pairs by larger logit first, then lower row index; NaN ranks
 // below every number. The high word is the logit's bit pattern made
@@ -275,6 +276,10 @@ __device__ __forceinline__ void argmax_combine(unsigned long long key, int lane,
     if (lane == 0 && valid_m) atomicMax(keys_m, key);
 }
 
+// Grid: gridDim.x = (number of clusters) * C; a cluster of C CTAs along x
+// shares tiles and splits K into C slices of kb_per super-blocks. With C > 1
+// every cluster owns exactly one tile. amax == nullptr: Y_i is written; else
+// (one matrix) no Y is written and each row's argmax key goes to amax[m].
 template <int MT, bool XB>
 __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks)
     gemv_kernel(const __grid_constant__ WeightGroup grp, const void* __restrict__ X, int M, int K,
