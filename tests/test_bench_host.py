@@ -1,0 +1,95 @@
+"""Host-side logic of bench.py that decides what the timed sweeps launch: which
+matrices form a grouped call, and where each matrix's outputs go."""
+import bench
+from gguf_q4_dequant_gb300 import synth
+
+
+def _names(wl):
+    return [(layer, m) for (layer, m, _, _) in synth.WORKLOADS[wl].matrices()]
+
+
+def test_groups_follow_shared_inputs():
+    names = _names(1)
+    groups = bench._group_spans(names)
+    assert [j for g in groups for j in g] == list(range(len(names)))  # a partition, in order
+    assert len(groups) == 4 * 16  # q/k/v, o, gate/up, down per layer
+    for g in groups:
+        ms = [names[j][1] for j in g]
+        assert ms in (["q_proj", "k_proj", "v_proj"], ["o_proj"], ["gate_proj", "up_proj"],
+                      ["down_proj"])
+        assert len({names[j][0] for j in g}) == 1  # never across layers
+
+
+def test_lm_head_is_its_own_call():
+    names = _names(2)
+    groups = bench._group_spans(names)
+    assert [names[j][1] for j in groups[-1]] == ["lm_head"]
+
+
+class _FakeLib:
+    def __init__(self):
+        self.calls = []
+
+    def q4k_matmul_multi(self, n, Ws, Ns, K, x, M, Ys, stream):
+        self.calls.append((M, [Ns[i] for i in range(n)], [Ys[i] for i in range(n)]))
+        return 0
+
+    q4k_matmul_multi_bf16 = q4k_matmul_multi
+
+
+class _FakeQ4K:
+    Q4KError = RuntimeError
+
+    def __init__(self):
+        self._lib = _FakeLib()
+
+    def lib(self):
+        return self._lib
+
+
+class _T:
+    """Stands in for a device tensor: only data_ptr() is used."""
+    def __init__(self, ptr):
+        self.ptr = ptr
+
+    def data_ptr(self):
+        return self.ptr
+
+
+def _outputs(wl, M):
+    w = synth.WORKLOADS[wl]
+    mats = [(_T(1 << 30), N, K) for (_, _, N, K) in w.matrices()]
+    names = _names(wl)
+    x = {K: _T(1 << 20) for (_, _, K) in mats}
+    base = 1 << 40
+    q4k = _FakeQ4K()
+    calls = bench._grouped_calls(q4k, mats, names, x, _T(base), 0, M=M, bf16=M > 16)
+    for c in calls:
+        c()
+    return q4k.lib().calls, base
+
+
+def test_decode_outputs_are_disjoint_slices():
+    """At M = 1 every matrix of the sweep writes its own slice of one buffer."""
+    calls, base = _outputs(1, 1)
+    spans = sorted((y - base, y - base + 4 * n) for (_, ns, ys) in calls for n, y in zip(ns, ys))
+    assert spans[0][0] == 0
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 == b0  # contiguous, no overlap
+    assert spans[-1][1] == 4 * sum(n for (_, _, n, _) in synth.WORKLOADS[1].matrices())
+
+
+def test_prefill_group_members_do_not_overlap():
+    """At M > 1 the matrices of one grouped call write disjoint M x N blocks that
+    fit the buffer _group_y_floats sizes; the groups reuse them."""
+    M = 512
+    calls, base = _outputs(3, M)
+    w = synth.WORKLOADS[3]
+    mats = [(None, N, K) for (_, _, N, K) in w.matrices()]
+    limit = 4 * bench._group_y_floats(mats, _names(3), M)
+    for (m, ns, ys) in calls:
+        assert m == M
+        spans = sorted((y - base, y - base + 4 * M * n) for n, y in zip(ns, ys))
+        for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+            assert a1 <= b0
+        assert spans[0][0] >= 0 and spans[-1][1] <= limit
