@@ -189,6 +189,31 @@ def test_gemm_long_k(q4k, oracle_mod):
     _check_matmul(q4k, oracle_mod, Wh, Wh.to(DEV), N, K, X, TOL_GEMM)
 
 
+def test_gemm_rows_beyond_one_launch(q4k, oracle_mod):
+    """More activation rows than one launch covers (65535 grid rows of the
+    narrowest 32-token tile): the call runs in row chunks, the last 5 rows long.
+    X repeats a block of P rows, P prime, so a chunk that read or wrote at the
+    wrong row offset would not line up with the expected rows."""
+    N, K, P = 130, 256, 4099
+    b = 65535 * 32  # first row of the second chunk
+    M = b + 5
+    Wh = synth.weight_rows(8100, N, K)
+    Xp = synth.activations(8101, P, K, torch.bfloat16)
+    X = Xp.to(DEV).repeat((M + P - 1) // P, 1)[:M].contiguous()
+    Y = torch.full((M, N), float("nan"), device=DEV)
+    q4k.matmul(Wh.to(DEV), N, K, X, Y)
+    torch.cuda.synchronize()
+    del X
+    assert bool(torch.isfinite(Y).all()), "unwritten or non-finite outputs"
+    Yref, A = oracle_mod.matmul(Wh.numpy(), N, K, _x_for_oracle(oracle_mod, Xp))
+    rng = np.random.default_rng(8102)
+    rows = sorted(set(range(40)) | set(range(b - 40, M)) | set(rng.integers(0, M, 200).tolist()))
+    got = Y[torch.as_tensor(rows, device=DEV)].cpu().double().numpy()
+    src = np.asarray(rows) % P
+    worst = float(np.max(np.abs(got - Yref[src]) / (TOL_GEMM * A[src] + 1e-30)))
+    assert worst <= 1.0, f"max |err| / ({TOL_GEMM} * sum|wx|) = {worst:.3f}"
+
+
 def test_dispatch_boundary_16_17(q4k, oracle_mod):
     N, K = 160, 512
     Wh = synth.weight_rows(7000, N, K)
