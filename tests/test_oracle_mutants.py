@@ -35,6 +35,14 @@ MUTANTS = {
                     "oracle_f16_to_f32((uint16_t)(blk[1] | (blk[0] << 8)))"),
     "x_transposed": ("const float* x = X + mi * K;", "const float* x = X + mi;"),
     "abs_dropped": ("aab += std::fabs(p);", "aab += p;"),
+    "sc_low_mask": ("sc[j] = s[j] & 63;", "sc[j] = s[j] & 127;"),
+    "high_nibble_sub_block": ("j_hi = 2 * c + 1", "j_hi = 2 * c"),
+    "min_of_other_sub_block": ("const float u_lo = dmin * (float)m[j_lo];",
+                               "const float u_lo = dmin * (float)m[j_hi];"),
+    "inf_nan_swapped": ("frac == 0 ? INFINITY : NAN", "frac == 0 ? NAN : INFINITY"),
+    "fp32_accumulator": ("acc += p;", "acc = (float)(acc + p);"),
+    "row_subset_ignored": ("const int64_t n = rows ? rows[r] : r;", "const int64_t n = r;"),
+    "last_thread_rows_dropped": ("r1 = std::min(nrows, r0 + per)", "r1 = std::min(nrows - 1, r0 + per)"),
     "row_layout": ("oracle_dequant_block(W + (n * KB + b) * 144, out + n * K + b * 256);",
                    "oracle_dequant_block(W + (b * N + n) * 144, out + n * K + b * 256);"),
 }
@@ -99,6 +107,7 @@ def _pins_fail(mod):
     """Run the pin checks against ``mod``; True if any of them fails."""
     checks = [lambda: [pins.test_hand_worked_blocks(mod, c) for c in pins._golden_cases()],
               lambda: pins.test_fp16_spot_values(mod),
+              lambda: pins.test_fp16_all_patterns_match_numpy(mod),
               lambda: pins.test_scale_bits_isolated(mod),
               lambda: pins.test_weights_are_the_exact_value_rounded_once(mod),
               lambda: pins.test_dequant_matrix_layout(mod),
