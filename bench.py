@@ -5,11 +5,14 @@ Metric: Q4_K dequant-matmul -- GEMV packed-weight GB/s (M=1); GEMM TFLOP/s (M=51
 A step is one pass of the hot path over one batch:
   * decode leg (the headline `value`): the Llama-3.2-1B-shaped sweep, 16
     layers x 7 Q4_K matrices (547 MB packed), M = 1 fp32 activation row,
-    112 GEMV launches replayed from a CUDA graph; value = packed weight bytes
-    per step / step time.
+    q/k/v and gate/up as grouped calls (64 GEMV launches), replayed from a
+    CUDA graph; value = packed weight bytes per step / step time. The same
+    sweep with one call per matrix (112 launches) and end to end from host
+    buffers are reported beside it, with the fused lm_head greedy pick.
   * prefill leg (`gemm`): the Qwen3-8B-shaped sweep, 36 layers x 7 matrices
-    (3.9 GB packed), M = 512 bf16 token rows, 252 tcgen05 GEMM launches;
-    value = 2*M*N*K flops per step / step time.
+    (3.9 GB packed), M = 512 bf16 token rows, grouped the same way (144
+    tcgen05 GEMM launches; 252 with one call per matrix); value = 2*M*N*K
+    flops per step / step time.
 Both weight sets are larger than L2, so every step streams weights from HBM.
 Inputs are synthetic (seeded generator), resident in HBM before timing.
 
@@ -169,14 +172,19 @@ class ClockSampler:
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path: str = ""):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.temporary = not path
+        if self.temporary:
+            import tempfile
+            fd, path = tempfile.mkstemp(prefix=f"q4k_clocks_rank{gpu_index}_", suffix=".csv")
+            os.close(fd)
+        self.path = path
         self.gpu = gpu_index
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
@@ -187,6 +195,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            if self.temporary and os.path.exists(self.path):
+                os.remove(self.path)
             return None
         self.proc.terminate()
         try:
@@ -204,6 +214,8 @@ class ClockSampler:
                     rows.append((float(parts[1]), float(parts[2]), float(parts[4]), parts[6:10]))
                 except ValueError:
                     continue
+        if self.temporary:
+            os.remove(self.path)
         if not rows:
             return None
         busy = [r for r in rows if r[2] > 0] or rows
@@ -448,7 +460,7 @@ def run_gpu(args):
     out = {"metric": METRIC, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic (seeded Q4_K weights, N(0,1) activations)"}
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, args.clocks_csv.replace("{rank}", str(rank)))
     sampler.start()
     launches = 0
     times = {}
@@ -602,7 +614,6 @@ def run_gpu(args):
 
     out["clocks"] = sampler.stop()
     times = max_over_ranks(times, ws, dev)
-    out.pop("_names1", None) if "decode" not in times else None
     out["device_error"] = q4k.q4k_device_error()
     out["gpu_launches"] = launches
     if rank != 0:
@@ -661,6 +672,9 @@ def main():
                     help="time every workload at every M / X dtype (one JSON line each)")
     ap.add_argument("--profile-bytes", type=float, default=300e6,
                     help="weight bytes to rotate through in --profile-shape (> L2)")
+    ap.add_argument("--clocks-csv", default="",
+                    help="keep the nvidia-smi clock samples in this file ('{rank}' is replaced "
+                         "by the rank; default: a temporary file)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

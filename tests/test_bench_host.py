@@ -93,3 +93,35 @@ def test_prefill_group_members_do_not_overlap():
         for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
             assert a1 <= b0
         assert spans[0][0] >= 0 and spans[-1][1] <= limit
+
+
+def test_clock_samples_are_summarised(tmp_path, monkeypatch):
+    """The clock record in the JSON line: median SM clock of the busy samples,
+    the maximum clock, and every throttle reason seen active (a stand-in
+    nvidia-smi on PATH prints fixed samples)."""
+    import os
+    import time
+    lines = [
+        "0, 345, 2070, 120.0, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1800, 2070, 1100.5, 100, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2000, 2070, 1000.0, 97, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1900, 2070, 1050.0, 100, 0x4, Not Active, Not Active, Not Active, Active",
+    ]
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\ncat <<'X'\n" + "\n".join(lines) + "\nX\nexec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    keep = tmp_path / "clocks.csv"
+    s = bench.ClockSampler(0, str(keep))
+    s.start()
+    for _ in range(100):  # until the stand-in has printed its samples
+        if keep.exists() and keep.read_text().count("\n") >= len(lines):
+            break
+        time.sleep(0.05)
+    rec = s.stop()
+    assert rec == {"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert keep.exists()  # a path given by the caller is kept
+    t = bench.ClockSampler(0)
+    t.start()
+    t.stop()
+    assert not os.path.exists(t.path)  # the default temporary file is removed
