@@ -453,7 +453,6 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             // K-slices of this cluster's tile: ranks 1.. push into rank 0, which adds in rank order
             if (rank != 0) {
                 const uint32_t dst = map_shared_rank(smem_u32(red + (rank - 1) * MT * kGemvTileRows), 0);
-#pragma unroll
                 const uint32_t rbar = map_shared_rank(bar_red, 0);
 #pragma unroll
                 for (int m = 0; m < ML; ++m) st_async_f32(dst + 4 * ((m0 + m) * kGemvTileRows + r), y[m], rbar);
