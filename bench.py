@@ -129,6 +129,55 @@ def cpu_oracle_decode(budget_s: float, threads: int):
                       f"{elapsed:.1f} s of CPU time"}
 
 
+def cpu_oracle_prefill(budget_s: float, threads: int, rows_per_matrix: int = 8):
+    """Times the oracle on the prefill workload (M = 512 bf16 token rows) over a
+    seeded subset of each matrix's output rows, in sweep order, until `budget_s`
+    seconds of oracle time; reports ns per (weight x token) and the full sweep
+    time that rate implies (labelled as extrapolated)."""
+    import numpy as np
+    import torch
+    import oracle
+    from gguf_q4_dequant_gb300 import synth
+    oracle.build()
+    w = synth.WORKLOADS[PREFILL_WL]
+    mats = w.matrices()
+    xs = {}
+    rng = np.random.default_rng(PREFILL_WL)
+    elapsed, done, wt = 0.0, 0, 0
+    while elapsed < budget_s and done < len(mats):
+        layer, name, N, K = mats[done]
+        if K not in xs:
+            xb = synth.activations(synth.x_seed(PREFILL_WL, K, PREFILL_M), PREFILL_M, K, torch.bfloat16)
+            xs[K] = oracle.bf16_to_f32(xb.view(torch.int16).numpy().view(np.uint16))
+        rows = sorted(rng.choice(N, size=rows_per_matrix, replace=False).tolist())
+        Wr = synth.weight_sample_rows(synth.weight_seed(PREFILL_WL, layer, name), N, K, rows).numpy()
+        t0 = time.perf_counter()
+        oracle.matmul(Wr, len(rows), K, xs[K], threads=threads)
+        elapsed += time.perf_counter() - t0
+        wt += len(rows) * K * PREFILL_M
+        done += 1
+    ns = elapsed / wt * 1e9
+    full = sum(N * K for (_, _, N, K) in mats) * PREFILL_M
+    return {"ns_per_weight_token": round(ns, 4), "cores": threads,
+            "extrapolated_s_per_sweep": round(ns * full * 1e-9, 1),
+            "extrapolated_tflops": round(2.0 / ns * 1e-3, 6),
+            "sample": f"oracle matmul over {rows_per_matrix} seeded output rows of each of the first "
+                      f"{done} matrices of the prefill sweep ({w.name}, M={PREFILL_M} bf16), "
+                      f"{elapsed:.1f} s of CPU time; the full-sweep time is extrapolated"}
+
+
+def cpu_baselines(budget_s: float):
+    """The oracle as it stands: the decode sweep on all host cores (the
+    reported value), the same on one thread, and a row sample of the prefill
+    workload on all host cores."""
+    cores = _host_cores()
+    cb = cpu_oracle_decode(budget_s, cores)
+    one = cpu_oracle_decode(max(1.0, budget_s / 4), 1)
+    cb["single_thread"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
+    cb["prefill"] = cpu_oracle_prefill(max(1.0, budget_s / 2), cores)
+    return cb
+
+
 def max_over_ranks(times, ws, device="cpu"):
     """Every timing as its maximum over the job's ranks (called by all ranks)."""
     import torch
@@ -645,7 +694,7 @@ def run_gpu(args):
     if args.layers:
         out["config"] = dict(out.get("config", {}), profiling_subset=f"first {args.layers} layers")
     if ws == 1 and not args.no_cpu_baseline and args.only == "all":
-        out["cpu_baseline"] = cpu_oracle_decode(args.cpu_budget, _host_cores())
+        out["cpu_baseline"] = cpu_baselines(args.cpu_budget)
     print(json.dumps(out))
 
 

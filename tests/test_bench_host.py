@@ -125,3 +125,15 @@ def test_clock_samples_are_summarised(tmp_path, monkeypatch):
     t.start()
     t.stop()
     assert not os.path.exists(t.path)  # the default temporary file is removed
+
+
+def test_prefill_oracle_sample_is_extrapolated_consistently():
+    """The prefill CPU baseline: a rate from sampled rows, and the full sweep
+    time implied by that rate over all 2*M*N*K of the workload."""
+    rec = bench.cpu_oracle_prefill(0.2, 2, rows_per_matrix=2)
+    ns = rec["ns_per_weight_token"]
+    assert ns > 0 and rec["cores"] == 2
+    w = synth.WORKLOADS[bench.PREFILL_WL]
+    full = sum(N * K for (_, _, N, K) in w.matrices()) * bench.PREFILL_M
+    assert abs(rec["extrapolated_s_per_sweep"] - ns * full * 1e-9) <= 0.051
+    assert "extrapolated" in rec["sample"]
