@@ -259,6 +259,62 @@ def test_full_size_sampled(q4k, oracle_mod, parity_record, wl):
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("wl,M,xdt", [(1, 1, "f32"), (3, 512, "bf16")])
+def test_benchmark_launches_layer0(q4k, oracle_mod, parity_record, wl, M, xdt):
+    """Layer 0 of the two benchmark sweeps, launched as bench.py times them:
+    q/k/v and gate/up as grouped calls built by the benchmark's own helper,
+    all calls of the layer in one CUDA graph on a side stream with programmatic
+    dependent launch (mode 2). Sampled output rows of every matrix are compared
+    with the oracle. Each group writes its own output buffer here, so no
+    group's outputs are overwritten by the next."""
+    import bench
+    bf16 = xdt == "bf16"
+    dt = torch.bfloat16 if bf16 else torch.float32
+    tol = TOL_GEMM if (bf16 and M > 16) else TOL_GEMV
+    _, mats, names = bench._weights(wl, DEV, 1, with_names=True)
+    Ks = sorted({K for (_, _, K) in mats})
+    xh = {K: synth.activations(synth.x_seed(wl, K, M), M, K, dt) for K in Ks}
+    xd = {K: xh[K].to(DEV) for K in Ks}
+    stream = torch.cuda.Stream()
+    groups = bench._group_spans(names)
+    ys, calls = [], []
+    for grp in groups:
+        sub = [mats[j] for j in grp]
+        yg = torch.empty(M * sum(N for (_, N, _) in sub), device=DEV)
+        cg = bench._grouped_calls(q4k, sub, [names[j] for j in grp], xd, yg, stream.cuda_stream,
+                                  M=M, bf16=bf16)
+        assert len(cg) == 1
+        ys.append(yg)
+        calls += cg
+    old = q4k.q4k_set_pdl(2)
+    try:
+        g = bench._capture(torch, calls, stream)
+        with torch.cuda.stream(stream):
+            for yg in ys:
+                yg.fill_(float("nan"))
+            g.replay()
+        torch.cuda.synchronize()
+    finally:
+        q4k.q4k_set_pdl(old)
+    for grp, yg in zip(groups, ys):
+        off = 0
+        for j in grp:
+            _, N, K = mats[j]
+            rows = _sample_rows(N, n=64)
+            W_rows = synth.weight_sample_rows(synth.weight_seed(wl, 0, names[j][1]), N, K, rows)
+            Yref, A = oracle_mod.matmul(W_rows.numpy(), len(rows), K, _x_for_oracle(oracle_mod, xh[K]))
+            got = yg[off:off + M * N].view(M, N)[:, torch.as_tensor(rows, device=DEV)]
+            got = got.cpu().double().numpy()
+            assert np.all(np.isfinite(got)), f"{names[j][1]}: unwritten outputs"
+            worst = float(np.max(np.abs(got - Yref) / (tol * A + 1e-30)))
+            assert worst <= 1.0, f"{names[j][1]}: max |err| / ({tol} * sum|wx|) = {worst:.3f}"
+            key = (wl, M, xdt)
+            parity_record[key] = max(parity_record.get(key, 0.0), worst)
+            off += M * N
+    del g, calls, ys, mats
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------ plumbing ---
 
 def test_outputs_stay_inside_y(q4k):
