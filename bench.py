@@ -156,9 +156,9 @@ def cpu_oracle_prefill(budget_s: float, threads: int, rows_per_matrix: int = 8):
         elapsed += time.perf_counter() - t0
         wt += len(rows) * K * PREFILL_M
         done += 1
-    ns = elapsed / wt * 1e9
+    ns = float(f"{elapsed / wt * 1e9:.6g}")
     full = sum(N * K for (_, _, N, K) in mats) * PREFILL_M
-    return {"ns_per_weight_token": round(ns, 4), "cores": threads,
+    return {"ns_per_weight_token": ns, "cores": threads,
             "extrapolated_s_per_sweep": round(ns * full * 1e-9, 1),
             "extrapolated_tflops": round(2.0 / ns * 1e-3, 6),
             "sample": f"oracle matmul over {rows_per_matrix} seeded output rows of each of the first "
