@@ -13,6 +13,15 @@ def test_stream_matches_scalar_definition():
         assert [v & synth.MASK64 for v in vals] == ref
 
 
+def test_stream_matches_published_splitmix64_outputs():
+    # The first outputs of Vigna's SplitMix64 seeded with 1234567, as listed with
+    # the published generator; the counter form value(seed, i) is output i.
+    published = [6457827717110365317, 3203168211198807973, 9817491932198370423,
+                 4593380528125082431, 16408922859458223821]
+    vals = [v & synth.MASK64 for v in synth.stream(1234567, 0, 5).tolist()]
+    assert vals == published
+
+
 def test_block_fields_and_ranges():
     blk = synth.blocks(synth.weight_seed(0, 0, "q_proj"), 0, 4096)
     assert blk.shape == (4096, 144) and blk.dtype == torch.uint8
