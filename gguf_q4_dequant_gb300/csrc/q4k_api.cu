@@ -232,7 +232,9 @@ const char* q4k_status_string(int status) {
     switch (status) {
         case Q4K_OK: return "Q4K_OK";
         case Q4K_ERR_NULL: return "Q4K_ERR_NULL: a required pointer is NULL";
-        case Q4K_ERR_BAD_DIM: return "Q4K_ERR_BAD_DIM: need N >= 1, M >= 1, K >= 256, K % 256 == 0";
+        case Q4K_ERR_BAD_DIM:
+            return "Q4K_ERR_BAD_DIM: a size or mode is out of range (N, M >= 1; K >= 256, K % 256 == 0; "
+                   "N, M < 2^31; K <= 2^24; group count 1..8; argmax M <= 16; PDL mode 0..2)";
         case Q4K_ERR_CUDA: return "Q4K_ERR_CUDA: a CUDA call or kernel launch failed";
         case Q4K_ERR_ALIGN: return "Q4K_ERR_ALIGN: W, X, Y and out must be 16-byte aligned";
         case Q4K_ERR_ARCH: return "Q4K_ERR_ARCH: the current device is not compute capability 10.3";

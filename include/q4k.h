@@ -54,7 +54,9 @@ extern "C" {
 enum q4k_status {
     Q4K_OK = 0,
     Q4K_ERR_NULL = -1,     /* a required pointer is NULL */
-    Q4K_ERR_BAD_DIM = -2,  /* N < 1, M < 1, K < 256 or K % 256 != 0, or too large */
+    Q4K_ERR_BAD_DIM = -2,  /* a size or mode out of range: needs N, M >= 1, K >= 256 and
+                              K % 256 == 0, N and M below 2^31, K <= 2^24, 1 <= count <= 8
+                              (grouped calls), M <= 16 (argmax calls), mode 0..2 (PDL) */
     Q4K_ERR_CUDA = -3,     /* a CUDA runtime call or kernel launch failed */
     Q4K_ERR_ALIGN = -4,    /* W, X, Y or out not 16-byte aligned */
     Q4K_ERR_ARCH = -5,     /* current device is not compute capability 10.3 */
