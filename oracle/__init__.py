@@ -1,7 +1,7 @@
 """CPU oracle for the packed Q4_K dequant-matmul -- TEST INFRASTRUCTURE ONLY.
 
 Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
-leg may import this package. The GPU library never imports or links it, and it
+and reference legs may import this package. The GPU library never imports or links it, and it
 shares no code with the GPU library.
 
 The arithmetic lives in ``q4k_oracle.cpp`` (plain C++, compiled here with gcc

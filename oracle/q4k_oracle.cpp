@@ -2,7 +2,7 @@
 //
 // TEST INFRASTRUCTURE ONLY. This file is the slow, obviously correct reference
 // that the GPU library is checked against. Only the test suite, the smoke check
-// and the benchmark's CPU-baseline leg may load it. It shares no code, header,
+// and the benchmark's CPU-baseline and reference legs may load it. It shares no code, header,
 // table or constant with the CUDA library, and it never calls it.
 //
 // What it computes (the Op::DequantMatMul of the rlx pages: "rlx-qwen3" crate
@@ -34,7 +34,8 @@
 // Parity pins (tests/test_oracle_pins.py): hand-worked blocks from
 // tests/golden/, per-bit isolation of all 96 scale bits, pack/unpack
 // round-trips, exact power-of-two weights, brute force against an independent
-// numpy matmul, and matmul invariants.
+// numpy matmul, and matmul invariants; tests/test_oracle_mutants.py plants
+// plausible mistakes in a copy of this file and checks that a pin catches each.
 
 #include <cmath>
 #include <cstdint>
