@@ -26,7 +26,7 @@ Q4K_ERR_TIMEOUT = -6
 #: every symbol include/q4k.h declares
 EXPORTS = ("q4k_status_string", "q4k_init", "q4k_dequant", "q4k_matmul", "q4k_matmul_bf16",
            "q4k_matmul_multi", "q4k_matmul_multi_bf16", "q4k_matmul_argmax",
-           "q4k_matmul_argmax_bf16", "q4k_set_pdl", "q4k_device_error")
+           "q4k_matmul_argmax_bf16", "q4k_set_pdl", "q4k_device_error", "q4k_selftest_timeout")
 MAX_GROUP = 8
 
 
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.q4k_set_pdl.restype = ctypes.c_int
             L.q4k_device_error.argtypes = [ctypes.c_int]
             L.q4k_device_error.restype = ctypes.c_int
+            L.q4k_selftest_timeout.argtypes = [i64, vp]
+            L.q4k_selftest_timeout.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -118,6 +120,29 @@ def _check_dtype(t, dtype, name):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _dims_valid(N, K, M=1):
+    return N >= 1 and M >= 1 and K >= 256 and K % 256 == 0
+
+
+def _check_size(t, need: int, name: str):
+    """A tensor (not a raw pointer) must hold at least `need` elements, so that
+    no kernel reads or writes past it."""
+    if t is not None and not isinstance(t, int) and t.numel() < need:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call needs {need}")
+
+
+def _w_bytes(N, K):
+    return N * (K // 256) * 144
+
+
+def _check_matmul_sizes(W, N, K, X, M, Y):
+    if not _dims_valid(N, K, M):
+        return  # the C ABI rejects the dimensions themselves
+    _check_size(W, _w_bytes(N, K), "W")
+    _check_size(X, M * K, "X")
+    _check_size(Y, M * N, "Y")
+
+
 def q4k_init():
     _check(lib().q4k_init(), "q4k_init")
 
@@ -127,6 +152,9 @@ def q4k_dequant(W, N: int, K: int, out, stream=None):
     import torch
     _check_dtype(W, torch.uint8, "W")
     _check_dtype(out, torch.float32, "out")
+    if _dims_valid(N, K):
+        _check_size(W, _w_bytes(N, K), "W")
+        _check_size(out, N * K, "out")
     _check(lib().q4k_dequant(_ptr(W), N, K, _ptr(out), _stream(stream)), "q4k_dequant")
 
 
@@ -136,6 +164,7 @@ def q4k_matmul(W, N: int, K: int, X, M: int, Y, stream=None):
     _check_dtype(W, torch.uint8, "W")
     _check_dtype(X, torch.float32, "X")
     _check_dtype(Y, torch.float32, "Y")
+    _check_matmul_sizes(W, N, K, X, M, Y)
     _check(lib().q4k_matmul(_ptr(W), N, K, _ptr(X), M, _ptr(Y), _stream(stream)), "q4k_matmul")
 
 
@@ -145,6 +174,7 @@ def q4k_matmul_bf16(W, N: int, K: int, X, M: int, Y, stream=None):
     _check_dtype(W, torch.uint8, "W")
     _check_dtype(X, torch.bfloat16, "X")
     _check_dtype(Y, torch.float32, "Y")
+    _check_matmul_sizes(W, N, K, X, M, Y)
     _check(lib().q4k_matmul_bf16(_ptr(W), N, K, _ptr(X), M, _ptr(Y), _stream(stream)),
            "q4k_matmul_bf16")
 
@@ -161,6 +191,8 @@ def q4k_matmul_multi(Ws, Ns, K: int, X, M: int, Ys, stream=None):
     bf16 = not isinstance(X, int) and X.dtype == torch.bfloat16
     if not bf16:
         _check_dtype(X, torch.float32, "X")
+    for W, N, Y in zip(Ws, Ns, Ys):
+        _check_matmul_sizes(W, int(N), K, X, M, Y)
     w_arr = (ctypes.c_void_p * count)(*[_ptr(W) for W in Ws])
     n_arr = (ctypes.c_int64 * count)(*[int(n) for n in Ns])
     y_arr = (ctypes.c_void_p * count)(*[_ptr(Y) for Y in Ys])
@@ -176,6 +208,9 @@ def q4k_matmul_argmax(W, N: int, K: int, X, M: int, out, stream=None):
     bf16 = not isinstance(X, int) and X.dtype == torch.bfloat16
     if not bf16:
         _check_dtype(X, torch.float32, "X")
+    _check_matmul_sizes(W, N, K, X, M, None)
+    if M >= 1:
+        _check_size(out, M, "out")
     fn = lib().q4k_matmul_argmax_bf16 if bf16 else lib().q4k_matmul_argmax
     _check(fn(_ptr(W), N, K, _ptr(X), M, _ptr(out), _stream(stream)), "q4k_matmul_argmax")
 
@@ -188,6 +223,13 @@ def argmax(W, N: int, K: int, X, out=None, stream=None):
         out = torch.empty(M, dtype=torch.int64, device=X.device)
     q4k_matmul_argmax(W, N, K, X, M, out, stream)
     return out
+
+
+def q4k_selftest_timeout(limit_ns: int, stream=None):
+    """Runs the one-thread kernel whose bounded wait runs out after limit_ns
+    (the library's timeout path, without a fault); q4k_device_error() then
+    reports Q4K_ERR_TIMEOUT."""
+    _check(lib().q4k_selftest_timeout(int(limit_ns), _stream(stream)), "q4k_selftest_timeout")
 
 
 def q4k_set_pdl(mode: int) -> int:

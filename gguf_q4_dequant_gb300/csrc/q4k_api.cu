@@ -3,11 +3,11 @@
 //
 // Dispatch (the decode / prefill split of the rlx-llama32 page's "Decode" and
 // "Packed GGUF" sections):
-//   q4k_dequant              -> K1 dequant_kernel
-//   q4k_matmul      M <= 16  -> K2 gemv_kernel (fp32 activations)
+//   q4k_dequant              -> K1 q4k_dequant_kernel
+//   q4k_matmul      M <= 16  -> K2 q4k_gemv_kernel (fp32 activations)
 //                   M >  16  -> K2 over consecutive 16-row slices of X
-//   q4k_matmul_bf16 M <= 16  -> K2 gemv_kernel (bf16 activations)
-//                   M >= 17  -> K3 gemm_kernel (tcgen05, TMEM accumulators)
+//   q4k_matmul_bf16 M <= 16  -> K2 q4k_gemv_kernel (bf16 activations)
+//                   M >= 17  -> K3 q4k_gemm_kernel (tcgen05, TMEM accumulators)
 //   q4k_matmul_multi[_bf16]  -> the same, for up to 8 matrices sharing K and X,
 //                   all of them in one launch (per 16-row slice for fp32 M > 16)
 //   q4k_matmul_argmax[_bf16] -> K2 with the fused argmax epilogue (M <= 16)
@@ -15,9 +15,11 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <memory>
 #include <mutex>
 
 #include "q4k.h"
+#include "q4k_device.cuh"
 #include "q4k_internal.h"
 
 namespace q4k {
@@ -25,6 +27,20 @@ namespace q4k {
 // Device error word: bit 0 = a bounded in-kernel wait ran out. Kernels receive
 // its device address (resolved per device in init_device).
 __device__ unsigned int g_device_error = 0;
+
+// The failure path of the bounded waits, on demand: one thread waits on an
+// mbarrier that nothing ever arrives at, with a short limit. The wait runs out,
+// sets the error word exactly as a timed-out pipeline wait would, and the
+// kernel returns. No copy or tensor-core operation is in flight.
+__global__ void q4k_selftest_timeout_kernel(unsigned long long limit_ns, unsigned int* err) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x == 0) {
+        const uint32_t b = smem_u32(&bar);
+        mbar_init(b, 1);
+        fence_barrier_init();
+        (void)mbar_wait(b, 0, err, limit_ns);
+    }
+}
 
 namespace {
 
@@ -71,7 +87,7 @@ void init_device(int dev, DeviceState& st) {
     st.info.num_sms = prop.multiProcessorCount;
     st.info.max_smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || gemv_setup() != cudaSuccess ||
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || gemv_setup(st.info) != cudaSuccess ||
         gemm_setup(st.info) != cudaSuccess || encoder() == nullptr) {
         st.status = Q4K_ERR_CUDA;
         return;
@@ -99,8 +115,42 @@ int check_dims(int64_t N, int64_t K) {
     return Q4K_OK;
 }
 
+// Encoded tensor maps, cached per host thread. A map is a pure function of the
+// base address, the tensor's dimensions and the box (everything else is fixed
+// per kind), so a cached map is valid for any later call with the same key --
+// whatever the memory holds by then. Direct-mapped: a collision re-encodes.
+// (A decode step issues one call per weight matrix, every token, with the same
+// pointers: the cache takes cuTensorMapEncodeTiled off that host path.)
+struct MapKey {
+    uintptr_t ptr;
+    int64_t a, b;
+    int box, kind;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && a == o.a && b == o.b && box == o.box && kind == o.kind;
+    }
+};
+struct MapEntry {
+    CUtensorMap map;
+    MapKey key;
+    bool valid;
+};
+constexpr int kMapCacheSize = 1024;
+
+MapEntry* map_slot(const MapKey& k) {
+    thread_local std::unique_ptr<MapEntry[]> cache;
+    if (!cache) {
+        cache.reset(new MapEntry[kMapCacheSize]);
+        for (int i = 0; i < kMapCacheSize; ++i) cache[i].valid = false;
+    }
+    uint64_t h = static_cast<uint64_t>(k.ptr >> 4) * 0x9E3779B97F4A7C15ull;
+    h ^= static_cast<uint64_t>(k.a) * 0xBF58476D1CE4E5B9ull;
+    h ^= static_cast<uint64_t>(k.b) * 0x94D049BB133111EBull;
+    h ^= static_cast<uint64_t>(k.box * 4 + k.kind);
+    return &cache[(h >> 40) % kMapCacheSize];
+}
+
 // W as a 2-D byte tensor {K/256*144, N}; box = one super-block of `rows` rows.
-int encode_w(CUtensorMap* map, const void* W, int64_t N, int64_t K, int rows) {
+int encode_w_uncached(CUtensorMap* map, const void* W, int64_t N, int64_t K, int rows) {
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 256) * 144;
     const cuuint64_t dims[2] = {row_bytes, static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {row_bytes};
@@ -112,8 +162,24 @@ int encode_w(CUtensorMap* map, const void* W, int64_t N, int64_t K, int rows) {
     return r == CUDA_SUCCESS ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
+int encode_w(CUtensorMap* map, const void* W, int64_t N, int64_t K, int rows) {
+    const MapKey key{reinterpret_cast<uintptr_t>(W), N, K, rows, 0};
+    MapEntry* e = map_slot(key);
+    if (e->valid && e->key == key) {
+        *map = e->map;
+        return Q4K_OK;
+    }
+    const int rc = encode_w_uncached(map, W, N, K, rows);
+    if (rc == Q4K_OK) {
+        e->map = *map;
+        e->key = key;
+        e->valid = true;
+    }
+    return rc;
+}
+
 // X as a 2-D bf16 tensor {K, M}; box {64, BN} with the 128-byte swizzle.
-int encode_x_bf16(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN) {
+int encode_x_bf16_uncached(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
     const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BN)};
@@ -123,6 +189,22 @@ int encode_x_bf16(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN)
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+int encode_x_bf16(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN) {
+    const MapKey key{reinterpret_cast<uintptr_t>(X), M, K, BN, 1};
+    MapEntry* e = map_slot(key);
+    if (e->valid && e->key == key) {
+        *map = e->map;
+        return Q4K_OK;
+    }
+    const int rc = encode_x_bf16_uncached(map, X, M, K, BN);
+    if (rc == Q4K_OK) {
+        e->map = *map;
+        e->key = key;
+        e->valid = true;
+    }
+    return rc;
 }
 
 // Tensor maps and the 128-row tile table of `count` matrices sharing K.
@@ -324,6 +406,16 @@ int q4k_matmul_argmax_bf16(const void* W, int64_t N, int64_t K, const uint16_t* 
 int q4k_set_pdl(int mode) {
     if (mode < 0 || mode > 2) return Q4K_ERR_BAD_DIM;
     return g_pdl.exchange(mode);
+}
+
+int q4k_selftest_timeout(int64_t limit_ns, void* stream) {
+    if (limit_ns < 1 || limit_ns > 1000000000LL) return Q4K_ERR_BAD_DIM;
+    const DeviceInfo* dev = nullptr;
+    const int rc = current_device(&dev);
+    if (rc != Q4K_OK) return rc;
+    q4k_selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<unsigned long long>(limit_ns), dev->err);
+    return cudaGetLastError() == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
 int q4k_device_error(int clear) {

@@ -13,7 +13,7 @@
 
 namespace q4k {
 
-__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ W,
+__global__ void __launch_bounds__(256) q4k_dequant_kernel(const uint8_t* __restrict__ W,
                                                       float* __restrict__ out, int64_t nblocks) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -60,7 +60,7 @@ cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, c
     const int64_t want = (nblocks + 7) / 8;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     const int grid = static_cast<int>(want < cap ? want : cap);
-    dequant_kernel<<<grid, threads, 0, stream>>>(W, out, nblocks);
+    q4k_dequant_kernel<<<grid, threads, 0, stream>>>(W, out, nblocks);
     return cudaGetLastError();
 }
 

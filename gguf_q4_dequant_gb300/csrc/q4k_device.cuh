@@ -15,6 +15,11 @@ constexpr int kBlockWeights = 256;  // weights per super-block
 
 // Time limit for any in-kernel wait; a correct pipeline waits microseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Limit for the waits a CTA makes on its way out after a timeout, for copies it
+// issued that nobody consumed: a bulk copy lands within microseconds, so once
+// this much time has passed it has landed even if the barrier it signals never
+// completes (because another role gave up before arriving on it).
+constexpr unsigned long long kDrainLimitNs = 1000000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
@@ -74,13 +79,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity to complete. Returns false
 // (and sets bit 0 of the device error word `err`) if it does not complete
-// within the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+// within `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+        if ((i & 63u) == 0 && globaltimer() - t0 > limit_ns) {
             atomicOr(err, 1u);
             return false;
         }

@@ -98,7 +98,7 @@ __device__ __forceinline__ uint4 dequant8x(uint64_t P, int hh, uint64_t d1s0, ui
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ WeightGroup grp, const __grid_constant__ CUtensorMap tmapX,
+    q4k_gemm_kernel(const __grid_constant__ WeightGroup grp, const __grid_constant__ CUtensorMap tmapX,
                 int M, int K, int C, int kb_per, int pdl_flags, unsigned int* err) {
     using Cfg = GemmCfg<BN>;
     constexpr int S = Cfg::kStages;
@@ -208,6 +208,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     atomicOr(err, 1u);
                     break;
                 }
+            }
+            // On a timeout the CTA must still not exit while a copy it issued is
+            // landing. A W stage (X step) is issued only after its previous use
+            // was released, which follows the landing of that use's bytes, so
+            // at most the last kGemmWStages W stages and S X steps issued can be
+            // in flight: wait for exactly those (the X steps' barriers also count
+            // the dequantisers' arrivals, hence the short limit: by then the
+            // copy has landed even if the dequantisers gave up).
+            if (sb < KB || ks < nks) {
+                for (int i = sb - kGemmWStages < 0 ? 0 : sb - kGemmWStages; i < sb; ++i)
+                    mbar_wait(bw_full + 8 * (i % kGemmWStages), (i / kGemmWStages) & 1, err, kDrainLimitNs);
+                for (int i = ks - S < 0 ? 0 : ks - S; i < ks; ++i)
+                    mbar_wait(bfull + 8 * (i % S), (i / S) & 1, err, kDrainLimitNs);
             }
         }
         __syncwarp();
@@ -366,6 +379,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        // every MMA this CTA issued has completed before its accumulator is
+        // freed (the epilogue's own wait is skipped after a timeout)
+        mbar_wait(bacc, 0, err);
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
     }
@@ -411,7 +427,7 @@ GemmPlan gemm_plan(int M, int ntiles, int K, const DeviceInfo& dev) {
 
 template <int BN>
 static cudaError_t setup_bn(DeviceInfo& dev, int bi) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(q4k_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          GemmCfg<BN>::kSmem);
     if (e != cudaSuccess) return e;
     for (int c = 1; c <= 8; ++c) {
@@ -427,7 +443,7 @@ static cudaError_t setup_bn(DeviceInfo& dev, int bi) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, q4k_gemm_kernel<BN>, &cfg) != cudaSuccess) {
             (void)cudaGetLastError();
             n = c == 1 ? dev.num_sms : 0;  // plain launches need no co-scheduling
         }
@@ -470,7 +486,7 @@ static cudaError_t launch_bn(const WeightGroup& grp, const CUtensorMap& tmapX, i
     cfg.attrs = attr;
     cfg.numAttrs = na;
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, grp, tmapX, M, K, plan.C, plan.kb_per, pdl_flags,
+    return cudaLaunchKernelEx(&cfg, q4k_gemm_kernel<BN>, grp, tmapX, M, K, plan.C, plan.kb_per, pdl_flags,
                               err);
 }
 

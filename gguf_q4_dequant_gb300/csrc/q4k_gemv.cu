@@ -77,8 +77,9 @@ struct GemvCfg {
     // cluster size, used only where its reduction slots stay small)
     static constexpr int kMaxSplit = MT <= 2 ? 16 : 8;
     static constexpr int kOffRed = kOffInv + kStages * MT * 2 * 4;       // ranks 1..: [kMaxSplit-1][m][128]
-    static constexpr int kOffBar = kOffRed + (kMaxSplit - 1) * MT * kGemvTileRows * 4;  // full[S], empty[S], red
-    static constexpr int kSmem = kOffBar + (2 * kStages + 1) * 8 + 128;  // + alignment slack
+    // wfull[S] (the stage's weight bytes), xfull[S] (its activations), empty[S], red
+    static constexpr int kOffBar = kOffRed + (kMaxSplit - 1) * MT * kGemvTileRows * 4;
+    static constexpr int kSmem = kOffBar + (3 * kStages + 1) * 8 + 128;  // + alignment slack
 };
 
 // Loads 8 consecutive activations of row m as fp32 (zeros past M).
@@ -282,7 +283,7 @@ __device__ __forceinline__ void argmax_combine(unsigned long long key, int lane,
 // (one matrix) no Y is written and each row's argmax key goes to amax[m].
 template <int MT, bool XB>
 __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks)
-    gemv_kernel(const __grid_constant__ WeightGroup grp, const void* __restrict__ X, int M, int K,
+    q4k_gemv_kernel(const __grid_constant__ WeightGroup grp, const void* __restrict__ X, int M, int K,
                 int C, int kb_per, int pdl_flags, unsigned long long* amax, unsigned int* err) {
     using Cfg = GemvCfg<MT>;
     constexpr int S = Cfg::kStages;
@@ -300,8 +301,12 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     const int nt_local = (tiles - cid + ncl - 1) / ncl;  // tiles cid, cid + ncl, ...
     const int total = nt_local * nb;                     // stages this CTA streams
 
-    const uint32_t bar_full = sbase + Cfg::kOffBar;
-    const uint32_t bar_empty = bar_full + 8 * S;
+    // a stage is ready when its weight bytes have landed (wfull: the producer's
+    // arrival and the TMA byte count) and its activations are staged (xfull);
+    // the producer can then drain its own copies without depending on others
+    const uint32_t bar_wfull = sbase + Cfg::kOffBar;
+    const uint32_t bar_xfull = bar_wfull + 8 * S;
+    const uint32_t bar_empty = bar_xfull + 8 * S;
     float* xs_ring = reinterpret_cast<float*>(smem + Cfg::kOffX);
     float* xsum_ring = reinterpret_cast<float*>(smem + Cfg::kOffXs);
     float* inv_ring = reinterpret_cast<float*>(smem + Cfg::kOffInv);
@@ -310,7 +315,8 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar_full + 8 * s, 1 + 32);  // producer (with bytes) + 32 activation lanes
+            mbar_init(bar_wfull + 8 * s, 1);   // producer, with the stage's bytes
+            mbar_init(bar_xfull + 8 * s, 32);  // the 32 activation lanes
             mbar_init(bar_empty + 8 * s, Cfg::kConsumers);  // every consumer warp reads every stage
         }
         // rank 0 of a cluster: the other ranks' partial sums land with
@@ -330,20 +336,25 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             for (int i = 0; i < grp.count; ++i) tma_prefetch_desc(&grp.maps[i]);
             if (pdl_flags & 1) pdl_wait();
             const uint64_t pol = policy_evict_first();
-            for (int st = 0; st < total; ++st) {
+            int issued = 0;
+            for (; issued < total; ++issued) {
+                const int st = issued;
                 const int s = st % S;
                 if (!mbar_wait(bar_empty + 8 * s, ((st / S) & 1) ^ 1, err)) break;
                 const int t = cid + (st / nb) * ncl;
                 const int mi = group_matrix(grp, t);
                 const int b = kb0 + st % nb;
-                mbar_arrive_expect_tx(bar_full + 8 * s, kGemvStageBytes);
+                mbar_arrive_expect_tx(bar_wfull + 8 * s, kGemvStageBytes);
                 tma_load_2d_hint(sbase + Cfg::kOffW + s * kGemvStageBytes, &grp.maps[mi],
                                  b * kBlockBytes, (t - grp.tile_start[mi]) * kGemvTileRows,
-                                 bar_full + 8 * s, pol);
+                                 bar_wfull + 8 * s, pol);
             }
-            // the CTA must not exit while a copy into its shared memory is in flight
-            for (int st = total - S < 0 ? 0 : total - S; st < total; ++st)
-                mbar_wait(bar_full + 8 * (st % S), (st / S) & 1, err);
+            // The CTA must not exit while a copy into its shared memory is in
+            // flight. Stage st is issued only after the consumers released stage
+            // st - S, which they do only after its bytes landed, so at most the
+            // last S issued stages can still be in flight: wait for exactly those.
+            for (int st = issued - S < 0 ? 0 : issued - S; st < issued; ++st)
+                mbar_wait(bar_wfull + 8 * (st % S), (st / S) & 1, err, kDrainLimitNs);
         }
         __syncwarp();
     } else if (warp == Cfg::kStagerWarp) {
@@ -399,7 +410,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 }
             }
             __syncwarp();
-            mbar_arrive(bar_full + 8 * s);
+            mbar_arrive(bar_xfull + 8 * s);
         }
     } else {
         // ------------------------------------------------------- consumers ---
@@ -413,26 +424,32 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
         float y[ML];
 #pragma unroll
         for (int m = 0; m < ML; ++m) y[m] = 0.f;
-        bool ok = true;  // after a timed-out wait the warp only keeps the barrier schedule
-        for (int i = 0; i < nt_local; ++i) {
+        // After a timed-out wait the warp stops: it releases no further stage,
+        // so the producer and the activation warp run out of time as well and
+        // nothing more is copied into this CTA. Waits are voted warp-uniform.
+        bool ok = true;
+        for (int i = 0; i < nt_local && ok; ++i) {
             for (int bl = 0; bl < nb; ++bl) {
                 const int st = i * nb + bl;
                 const int s = st % S;
-                ok = ok && mbar_wait(bar_full + 8 * s, (st / S) & 1, err);
-                if (ok) {
-                    float acc[ML];
-                    const uint8_t* P = smem + Cfg::kOffW + s * kGemvStageBytes + r * kBlockBytes;
-                    const float* xs = xs_ring + (s * MT + m0) * 256;
-                    const float* xsm = xsum_ring + (s * MT + m0) * 8;
-                    block_dot<ML>(P, xs, xsm, acc);
-                    const float* inv = inv_ring + (s * MT + m0) * 2;
-#pragma unroll
-                    for (int m = 0; m < ML; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
+                const uint32_t par = (st / S) & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_wfull + 8 * s, par, err) &&
+                                                 mbar_wait(bar_xfull + 8 * s, par, err))) {
+                    ok = false;
+                    break;
                 }
+                float acc[ML];
+                const uint8_t* P = smem + Cfg::kOffW + s * kGemvStageBytes + r * kBlockBytes;
+                const float* xs = xs_ring + (s * MT + m0) * 256;
+                const float* xsm = xsum_ring + (s * MT + m0) * 8;
+                block_dot<ML>(P, xs, xsm, acc);
+                const float* inv = inv_ring + (s * MT + m0) * 2;
+#pragma unroll
+                for (int m = 0; m < ML; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             }
-            if (C == 1) {  // C > 1: one tile per CTA, reduced across the cluster below
+            if (ok && C == 1) {  // C > 1: one tile per CTA, reduced across the cluster below
                 const int t = cid + i * ncl;
                 const int mi = group_matrix(grp, t);
                 const int row = (t - grp.tile_start[mi]) * kGemvTileRows + r;
@@ -450,13 +467,17 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             }
         }
         if (C > 1) {
-            // K-slices of this cluster's tile: ranks 1.. push into rank 0, which adds in rank order
+            // K-slices of this cluster's tile: ranks 1.. push into rank 0, which adds
+            // in rank order. A rank that timed out pushes nothing; rank 0 always
+            // waits (bounded) for the pushes before it exits, so none lands in the
+            // shared memory of a CTA that has gone.
             if (rank != 0) {
+                if (!ok) return;
                 const uint32_t dst = map_shared_rank(smem_u32(red + (rank - 1) * MT * kGemvTileRows), 0);
                 const uint32_t rbar = map_shared_rank(bar_red, 0);
 #pragma unroll
                 for (int m = 0; m < ML; ++m) st_async_f32(dst + 4 * ((m0 + m) * kGemvTileRows + r), y[m], rbar);
-            } else if (__all_sync(0xffffffffu, mbar_wait(bar_red, 0, err))) {  // warp-uniform (argmax shuffles)
+            } else if (__all_sync(0xffffffffu, mbar_wait(bar_red, 0, err)) && ok) {  // warp-uniform (argmax shuffles)
                 const int mi = group_matrix(grp, cid);
                 const int row = (cid - grp.tile_start[mi]) * kGemvTileRows + r;
                 const int Nm = grp.N[mi];
@@ -481,23 +502,18 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
 
 // ------------------------------------------------------------------ host ---
 
-namespace {
-int g_occ[2][5];           // resident CTAs per SM for each (XB, MT) instantiation
-int g_clusters[2][5][17];  // resident clusters of C CTAs (C = 2..kMaxSplit), same index
-}
-
 template <int MT, bool XB>
-static cudaError_t set_attr(int slot) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT, XB>,
+static cudaError_t set_attr(DeviceInfo& dev, int slot) {
+    cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, XB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<MT>::kSmem);
     if (e != cudaSuccess) return e;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<MT, XB>, GemvCfg<MT>::kThreads,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, q4k_gemv_kernel<MT, XB>, GemvCfg<MT>::kThreads,
                                                       GemvCfg<MT>::kSmem);
-    g_occ[XB ? 1 : 0][slot] = occ < 1 ? 1 : occ;
+    dev.gemv_occ[XB ? 1 : 0][slot] = occ < 1 ? 1 : occ;
     if (e != cudaSuccess) return e;
     if (GemvCfg<MT>::kMaxSplit > 8 &&
-        cudaFuncSetAttribute(gemv_kernel<MT, XB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaFuncSetAttribute(q4k_gemv_kernel<MT, XB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess)
         (void)cudaGetLastError();  // then the occupancy query below reports 0 for C > 8
     for (int c = 2; c <= GemvCfg<MT>::kMaxSplit; ++c) {
@@ -513,21 +529,21 @@ static cudaError_t set_attr(int slot) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<MT, XB>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, q4k_gemv_kernel<MT, XB>, &cfg) != cudaSuccess) {
             (void)cudaGetLastError();
             n = 0;
         }
-        g_clusters[XB ? 1 : 0][slot][c] = n;
+        dev.gemv_clusters[XB ? 1 : 0][slot][c] = n;
     }
     return cudaSuccess;
 }
 
-cudaError_t gemv_setup() {
+cudaError_t gemv_setup(DeviceInfo& dev) {
     cudaError_t e = cudaSuccess;
     cudaError_t r;
-#define Q4K_SET(MT, SLOT)                                           \
-    if ((r = set_attr<MT, false>(SLOT)) != cudaSuccess) e = r;      \
-    if ((r = set_attr<MT, true>(SLOT)) != cudaSuccess) e = r;
+#define Q4K_SET(MT, SLOT)                                                \
+    if ((r = set_attr<MT, false>(dev, SLOT)) != cudaSuccess) e = r;      \
+    if ((r = set_attr<MT, true>(dev, SLOT)) != cudaSuccess) e = r;
     Q4K_SET(1, 0) Q4K_SET(2, 1) Q4K_SET(4, 2) Q4K_SET(8, 3) Q4K_SET(16, 4)
 #undef Q4K_SET
     return e;
@@ -538,7 +554,7 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
                              const DeviceInfo& dev, int slot, int pdl, unsigned long long* amax) {
     const int KB = K / kBlockWeights;
     const int tiles = grp.tile_start[grp.count];
-    const int slots = dev.num_sms * g_occ[XB ? 1 : 0][slot];
+    const int slots = dev.num_sms * dev.gemv_occ[XB ? 1 : 0][slot];
     int C = 1, kb_per = KB, grid;
     if (tiles >= slots) {
         // persistent, one CTA per resident slot (CTA c streams tiles c, c + grid,
@@ -556,7 +572,7 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
         for (; c >= 2; --c) {
             const int kp = (KB + c - 1) / c;
             const int ce = (KB + kp - 1) / kp;
-            if (g_clusters[XB ? 1 : 0][slot][ce] >= tiles) {
+            if (dev.gemv_clusters[XB ? 1 : 0][slot][ce] >= tiles) {
                 C = ce;
                 kb_per = kp;
                 break;
@@ -588,7 +604,7 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
     // pdl_flags bit 0: the producer also waits for the preceding grid before
     // streaming W (cleared only when the caller allows weight prefetch).
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, XB>, grp, X, M, K, C, kb_per, pdl_flags, amax,
+    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, XB>, grp, X, M, K, C, kb_per, pdl_flags, amax,
                               dev.err);
 }
 
@@ -607,19 +623,19 @@ cudaError_t launch_gemv(const WeightGroup& grp, const void* X, bool x_bf16, int 
 }
 
 // Keys of the fused argmax: cleared before the GEMV, turned into row indices after it.
-__global__ void argmax_init_kernel(unsigned long long* keys, int M) {
+__global__ void q4k_argmax_init_kernel(unsigned long long* keys, int M) {
     if (static_cast<int>(threadIdx.x) < M) keys[threadIdx.x] = 0ull;
 }
-__global__ void argmax_finish_kernel(unsigned long long* keys, int M) {
+__global__ void q4k_argmax_finish_kernel(unsigned long long* keys, int M) {
     if (static_cast<int>(threadIdx.x) < M) keys[threadIdx.x] = 0xFFFFFFFFull - (keys[threadIdx.x] & 0xFFFFFFFFull);
 }
 
 cudaError_t launch_argmax_init(unsigned long long* keys, int M, cudaStream_t stream) {
-    argmax_init_kernel<<<1, 32, 0, stream>>>(keys, M);
+    q4k_argmax_init_kernel<<<1, 32, 0, stream>>>(keys, M);
     return cudaGetLastError();
 }
 cudaError_t launch_argmax_finish(unsigned long long* keys, int M, cudaStream_t stream) {
-    argmax_finish_kernel<<<1, 32, 0, stream>>>(keys, M);
+    q4k_argmax_finish_kernel<<<1, 32, 0, stream>>>(keys, M);
     return cudaGetLastError();
 }
 

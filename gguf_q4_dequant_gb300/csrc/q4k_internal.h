@@ -15,6 +15,10 @@ struct DeviceInfo {
     // GEMM: clusters of C CTAs that can be resident at once, per tile width
     // BN = 32 << i (i < 4) and split C (index C, 1..8), from the occupancy API.
     int gemm_clusters[4][9] = {};
+    // GEMV, per (bf16 activations?, M slot 1/2/4/8/16): resident CTAs per SM,
+    // and resident clusters of C CTAs (index C, 2..16).
+    int gemv_occ[2][5] = {};
+    int gemv_clusters[2][5][17] = {};
 };
 
 cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, cudaStream_t stream,
@@ -50,7 +54,8 @@ cudaError_t launch_gemv(const WeightGroup& grp, const void* X, bool x_bf16, int 
                         unsigned long long* amax = nullptr);
 cudaError_t launch_argmax_init(unsigned long long* keys, int M, cudaStream_t stream);
 cudaError_t launch_argmax_finish(unsigned long long* keys, int M, cudaStream_t stream);
-cudaError_t gemv_setup();
+// Sets the kernels' attributes and fills dev.gemv_occ / dev.gemv_clusters.
+cudaError_t gemv_setup(DeviceInfo& dev);
 
 // tcgen05 GEMM for M >= 17 rows of bf16 activations over a group of weight
 // matrices (grp.maps as for the GEMV); tmapX: 2-D bf16 map {K, M}, box

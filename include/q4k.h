@@ -83,18 +83,29 @@ int q4k_init(void);
 int q4k_dequant(const void* W, int64_t N, int64_t K, float* out_f32, void* stream);
 
 /*
- * Y = X * W^T with fp32 activations X [M][K].
+ * Y = X * W^T with fp32 activations X [M][K]: the packed-weight matmul that
+ * each linear layer of a K-quant model emits ("rlx-qwen3" crate page, the
+ * packed-GGUF note under "Quick start"; "rlx-llama32" crate page, section
+ * "Packed GGUF"), with the weights dequantised inside the kernel.
  * M <= 16 (decode) runs the split-K GEMV kernel; larger M runs it over
- * 16-row slices of X. Accuracy: |Y - exact| <= 1e-4 * sum_k |X*w| per output.
+ * 16-row slices of X, which reads W once per slice (fp32 prefill costs
+ * ceil(M/16) weight sweeps; bf16 activations through q4k_matmul_bf16 read W
+ * once). Accuracy: |Y - exact| <= 1e-4 * sum_k |X*w| per output.
+ *   W  device, N*K/256*144 bytes; X device, M*K floats; Y device, M*N floats;
+ *   all 16-byte aligned.
  */
 int q4k_matmul(const void* W, int64_t N, int64_t K, const float* X, int64_t M, float* Y,
                void* stream);
 
 /*
- * Y = X * W^T with bfloat16 activations X_bf16 [M][K] (bit patterns).
- * M <= 16 runs the split-K GEMV kernel (accuracy 1e-4 * sum|X*w|); M >= 17
- * (chunked prefill) runs the tcgen05 tensor-core GEMM, which rounds the
- * dequantised weights to bfloat16 (accuracy 5e-3 * sum|X*w|).
+ * Y = X * W^T with bfloat16 activations X_bf16 [M][K] (bit patterns): the same
+ * packed-weight matmul ("rlx-llama32" crate page, section "Packed GGUF") for a
+ * block of token rows, as the chunked prefill of the nx_f32_llm_run_v3 listing
+ * issues it. M <= 16 runs the split-K GEMV kernel (accuracy 1e-4 *
+ * sum|X*w|); M >= 17 (chunked prefill) runs the tcgen05 tensor-core GEMM,
+ * which rounds the dequantised weights to bfloat16 (accuracy 5e-3 * sum|X*w|).
+ *   W  device, N*K/256*144 bytes; X_bf16 device, M*K uint16; Y device, M*N
+ *   floats; all 16-byte aligned.
  */
 int q4k_matmul_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16, int64_t M,
                     float* Y, void* stream);
@@ -153,6 +164,18 @@ int q4k_set_pdl(int mode);
  * clear != 0 the word is reset. Not capturable.
  */
 int q4k_device_error(int clear);
+
+/*
+ * Exercises the failure path of the in-kernel waits without any fault: one
+ * thread of a one-warp kernel waits on an mbarrier that nothing arrives at,
+ * bounded by limit_ns nanoseconds (1 .. 10^9). The wait runs out, sets the
+ * device error word as a timed-out wait in any libq4k kernel does, and the
+ * kernel returns; no copy or tensor-core work is in flight, so the context
+ * stays usable. Afterwards q4k_device_error() reports Q4K_ERR_TIMEOUT. For
+ * tests of error handling; asynchronous on `stream`. (The pages describe no
+ * such call: it checks this library's own timeout mechanism.)
+ */
+int q4k_selftest_timeout(int64_t limit_ns, void* stream);
 
 #ifdef __cplusplus
 }

@@ -131,3 +131,36 @@ def test_argmax_host_checks(q4k):
         assert f(A16, 4, 300, A16, 1, A16, None) == q4k.Q4K_ERR_BAD_DIM
         assert f(A16, 4, 256, A16, 1, A16 + 4, None) == q4k.Q4K_ERR_ALIGN  # int64 out: 8-byte aligned
         assert f(A16, 4, 256, A16 + 8, 1, A16, None) == q4k.Q4K_ERR_ALIGN
+
+
+def test_selftest_timeout_rejects_bad_limits(q4k):
+    L = q4k.lib()
+    for limit in (0, -5, 1_000_000_001):
+        assert L.q4k_selftest_timeout(limit, None) == q4k.Q4K_ERR_BAD_DIM
+
+
+def test_binding_checks_tensor_sizes(q4k):
+    """A tensor shorter than the call needs is refused before the C ABI is
+    reached (the kernels would read or write past it)."""
+    torch = pytest.importorskip("torch")
+    N, K, M = 4, 512, 3
+    W = torch.zeros(N * (K // 256) * 144, dtype=torch.uint8)
+    X = torch.zeros(M, K)
+    Y = torch.zeros(M, N)
+    cases = [
+        lambda: q4k.q4k_matmul(W[:-16], N, K, X, M, Y),
+        lambda: q4k.q4k_matmul(W, N, K, X[:2], M, Y),
+        lambda: q4k.q4k_matmul(W, N, K, X, M, Y[:, :3].contiguous()),
+        lambda: q4k.q4k_matmul_bf16(W, N, K, X.to(torch.bfloat16)[:1], M, Y),
+        lambda: q4k.q4k_dequant(W, N, K, torch.zeros(N * K - 1)),
+        lambda: q4k.q4k_dequant(W[:100], N, K, torch.zeros(N * K)),
+        lambda: q4k.q4k_matmul_multi([W, W[:10]], [N, N], K, X, M, [Y, Y]),
+        lambda: q4k.q4k_matmul_multi([W, W], [N, N], K, X, M, [Y, Y[:1]]),
+        lambda: q4k.q4k_matmul_argmax(W, N, K, X, M, torch.zeros(M - 1, dtype=torch.int64)),
+    ]
+    for call in cases:
+        with pytest.raises(ValueError, match="the call needs"):
+            call()
+    # right sizes pass the size checks and stop at the device check (host tensors)
+    with pytest.raises(ValueError, match="CUDA device memory"):
+        q4k.q4k_matmul(W, N, K, X, M, Y)
