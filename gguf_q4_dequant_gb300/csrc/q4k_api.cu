@@ -44,6 +44,18 @@ __global__ void q4k_selftest_timeout_kernel(unsigned long long limit_ns, unsigne
 
 namespace {
 
+// Decode products with at least this many activation rows (and at most 16)
+// run on the tensor cores (K4); fewer run on the CUDA cores (K2).
+#ifndef Q4K_TC_MIN_M
+#define Q4K_TC_MIN_M 5
+#endif
+
+cudaError_t launch_decode(const WeightGroup& grp, const void* X, bool xb, int M, int K, cudaStream_t stream,
+                          const DeviceInfo& dev, int pdl, unsigned long long* amax = nullptr) {
+    if (M >= Q4K_TC_MIN_M) return launch_tcgemv(grp, X, xb, M, K, stream, dev, pdl, amax);
+    return launch_gemv(grp, X, xb, M, K, stream, dev, pdl, amax);
+}
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
@@ -87,7 +99,7 @@ void init_device(int dev, DeviceState& st) {
     st.info.num_sms = prop.multiProcessorCount;
     st.info.max_smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || gemv_setup(st.info) != cudaSuccess ||
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || gemv_setup(st.info) != cudaSuccess || tcgemv_setup(st.info) != cudaSuccess ||
         gemm_setup(st.info) != cudaSuccess || encoder() == nullptr) {
         st.status = Q4K_ERR_CUDA;
         return;
@@ -231,8 +243,8 @@ int run_gemv(int count, const void* const* W, const int64_t* N, int64_t K, const
         const int mc = static_cast<int>(M - m0 < 16 ? M - m0 : 16);
         const void* Xc = static_cast<const uint8_t*>(X) + static_cast<size_t>(m0) * K * xelem;
         for (int i = 0; i < count; ++i) grp.Y[i] = Y[i] + m0 * N[i];
-        if (launch_gemv(grp, Xc, xb, mc, static_cast<int>(K), stream, dev,
-                        g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
+        if (launch_decode(grp, Xc, xb, mc, static_cast<int>(K), stream, dev,
+                          g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
             return Q4K_ERR_CUDA;
     }
     return Q4K_OK;
@@ -270,8 +282,8 @@ int run_argmax(const void* W, int64_t N, int64_t K, const void* X, bool xb, int6
     auto* keys = reinterpret_cast<unsigned long long*>(out);
     const int m = static_cast<int>(M);
     if (launch_argmax_init(keys, m, stream) != cudaSuccess ||
-        launch_gemv(grp, X, xb, m, static_cast<int>(K), stream, dev,
-                    g_pdl.load(std::memory_order_relaxed), keys) != cudaSuccess ||
+        launch_decode(grp, X, xb, m, static_cast<int>(K), stream, dev,
+                      g_pdl.load(std::memory_order_relaxed), keys) != cudaSuccess ||
         launch_argmax_finish(keys, m, stream) != cudaSuccess)
         return Q4K_ERR_CUDA;
     return Q4K_OK;

@@ -258,6 +258,34 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)
         : "r"(taddr)
         : "memory");
 }
+// 32 lanes x N consecutive 32-bit columns (N = 2, 4, 8, 16) from TMEM into registers.
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&v)[2]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
+                 : "=r"(v[0]), "=r"(v[1])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&v)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&v)[32]) {
+    tmem_ld_32x32b_x32(taddr, v);
+}
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -283,6 +311,31 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | (1u << 10)                                // B format: bf16
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// ------------------------------------------------------ fused argmax ---
+
+// Argmax of a row of Y (fused lm_head + greedy pick): a 64-bit key that orders
+// (logit, row) pairs by larger logit first, then lower row index; NaN ranks
+// below every number. The high word is the logit's bit pattern made
+// order-preserving as an unsigned integer, the low word the row's complement.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
+    const uint32_t u = __float_as_uint(v);
+    uint32_t hi = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    if (v != v) hi = 0u;
+    return (static_cast<unsigned long long>(hi) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(n));
+}
+
+// The warp's largest key, combined into keys[m] (the maximum does not depend on
+// the order in which warps arrive, so the result is deterministic).
+__device__ __forceinline__ void argmax_combine(unsigned long long key, int lane, bool valid_m,
+                                               unsigned long long* keys_m) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long t = __shfl_xor_sync(0xffffffffu, key, o);
+        key = t > key ? t : key;
+    }
+    if (lane == 0 && valid_m) atomicMax(keys_m, key);
 }
 
 // ------------------------------------------------------------ cluster ---

@@ -53,6 +53,19 @@ constexpr int kGemvTileRows = 128;
 constexpr int kGemvConsumers = 4;  // consumer warps: one lane per row of the tile
 constexpr int kGemvStageBytes = kGemvTileRows * kBlockBytes;  // 18432
 
+#ifndef Q4K_GEMV_SGROUPS
+#define Q4K_GEMV_SGROUPS 2
+#endif
+#ifndef Q4K_GEMV_STAGES
+#define Q4K_GEMV_STAGES 4
+#endif
+#ifndef Q4K_GEMV_MINB
+#define Q4K_GEMV_MINB 2
+#endif
+#ifndef Q4K_GEMV_GRIDOCC
+#define Q4K_GEMV_GRIDOCC 0
+#endif
+
 template <int MT>
 struct GemvCfg {
     // M >= 8: two groups of consumer warps on the same rows and stages, each
@@ -60,15 +73,20 @@ struct GemvCfg {
     // accumulators fit and twice as many warps share the FMA work
     static constexpr int kMGroups = MT >= 8 ? 2 : 1;
     static constexpr int kML = MT / kMGroups;
-    static constexpr int kConsumers = kGemvConsumers * kMGroups;
+    // M <= 2: kSGroups groups of consumer warps take alternate stages of the
+    // same tile (more warps to hide latency); their partial sums are added at
+    // the end of the tile, group 0 + group 1 (deterministic)
+    static constexpr int kSGroups = MT <= 2 ? Q4K_GEMV_SGROUPS : 1;
+    static constexpr int kStageConsumers = kGemvConsumers * kMGroups;  // warps reading a stage
+    static constexpr int kConsumers = kStageConsumers * kSGroups;
     static constexpr int kProducerWarp = kConsumers;
     static constexpr int kStagerWarp = kConsumers + 1;
     static constexpr int kThreads = 32 * (kConsumers + 2);
     // registers: two resident CTAs per SM for small M (measured: more registers
     // per thread buy more overlap than a third CTA would); M >= 8 takes ~145-165
     // registers a thread at 320 threads, one CTA per SM
-    static constexpr int kMinBlocks = MT >= 8 ? 1 : 2;
-    static constexpr int kStages = 4;
+    static constexpr int kMinBlocks = MT >= 8 ? 1 : (MT <= 2 ? Q4K_GEMV_MINB : 2);
+    static constexpr int kStages = MT <= 2 ? Q4K_GEMV_STAGES : 4;
     static constexpr int kOffW = 0;
     static constexpr int kOffX = kOffW + kStages * kGemvStageBytes;     // x' [stage][m][256]
     static constexpr int kOffXs = kOffX + kStages * MT * 256 * 4;        // sums [stage][m][8]
@@ -77,9 +95,12 @@ struct GemvCfg {
     // cluster size, used only where its reduction slots stay small)
     static constexpr int kMaxSplit = MT <= 2 ? 16 : 8;
     static constexpr int kOffRed = kOffInv + kStages * MT * 2 * 4;       // ranks 1..: [kMaxSplit-1][m][128]
-    // wfull[S] (the stage's weight bytes), xfull[S] (its activations), empty[S], red
-    static constexpr int kOffBar = kOffRed + (kMaxSplit - 1) * MT * kGemvTileRows * 4;
-    static constexpr int kSmem = kOffBar + (3 * kStages + 1) * 8 + 128;  // + alignment slack
+    // stage groups 1..: their partial sums of a tile, [kSGroups-1][m][128]
+    static constexpr int kOffComb = kOffRed + (kMaxSplit - 1) * MT * kGemvTileRows * 4;
+    // wfull[S] (the stage's weight bytes), xfull[S] (its activations), empty[S],
+    // red, comb_full, comb_empty
+    static constexpr int kOffBar = kOffComb + (kSGroups - 1) * MT * kGemvTileRows * 4;
+    static constexpr int kSmem = kOffBar + (3 * kStages + 3) * 8 + 128;  // + alignment slack
 };
 
 // Loads 8 consecutive activations of row m as fp32 (zeros past M).
@@ -254,29 +275,6 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
     }
 }
 
-// Argmax of a row of Y (fused lm_head + greedy pick): a 64-bit key that orders
-// (logit, row) pairs by larger logit first, then lower row index; NaN ranks
-// below every number. The high word is the logit's bit pattern made
-// order-preserving as an unsigned integer, the low word the row's complement.
-__device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
-    const uint32_t u = __float_as_uint(v);
-    uint32_t hi = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    if (v != v) hi = 0u;
-    return (static_cast<unsigned long long>(hi) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(n));
-}
-
-// The warp's largest key, combined into keys[m] (the maximum does not depend on
-// the order in which warps arrive, so the result is deterministic).
-__device__ __forceinline__ void argmax_combine(unsigned long long key, int lane, bool valid_m,
-                                               unsigned long long* keys_m) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long t = __shfl_xor_sync(0xffffffffu, key, o);
-        key = t > key ? t : key;
-    }
-    if (lane == 0 && valid_m) atomicMax(keys_m, key);
-}
-
 // Grid: gridDim.x = (number of clusters) * C; a cluster of C CTAs along x
 // shares tiles and splits K into C slices of kb_per super-blocks. With C > 1
 // every cluster owns exactly one tile. amax == nullptr: Y_i is written; else
@@ -312,13 +310,17 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
     float* inv_ring = reinterpret_cast<float*>(smem + Cfg::kOffInv);
     float* red = reinterpret_cast<float*>(smem + Cfg::kOffRed);
     const uint32_t bar_red = bar_empty + 8 * S;
+    const uint32_t bar_cfull = bar_red + 8, bar_cempty = bar_red + 16;
+    float* comb = reinterpret_cast<float*>(smem + Cfg::kOffComb);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_wfull + 8 * s, 1);   // producer, with the stage's bytes
             mbar_init(bar_xfull + 8 * s, 32);  // the 32 activation lanes
-            mbar_init(bar_empty + 8 * s, Cfg::kConsumers);  // every consumer warp reads every stage
+            mbar_init(bar_empty + 8 * s, Cfg::kStageConsumers);  // the warps of one stage group
         }
+        mbar_init(bar_cfull, 32 * Cfg::kStageConsumers);   // every lane of stage group 1
+        mbar_init(bar_cempty, 32 * Cfg::kStageConsumers);  // every lane of stage group 0
         // rank 0 of a cluster: the other ranks' partial sums land with
         // st.async and count their bytes; rank 0's own arrival carries the total
         mbar_init(bar_red, 1);
@@ -419,8 +421,10 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
         // while the stage ring fills, rather than after the compute)
         if (C > 1) cluster_wait();
         constexpr int ML = Cfg::kML;
-        const int r = 32 * (warp % kGemvConsumers) + lane;  // row within the tile
-        const int m0 = (warp / kGemvConsumers) * ML;        // first activation row of this warp
+        constexpr int SG = Cfg::kSGroups;
+        const int sg = warp / Cfg::kStageConsumers;                   // stage group
+        const int r = 32 * (warp % kGemvConsumers) + lane;            // row within the tile
+        const int m0 = ((warp / kGemvConsumers) % Cfg::kMGroups) * ML;  // first activation row
         float y[ML];
 #pragma unroll
         for (int m = 0; m < ML; ++m) y[m] = 0.f;
@@ -428,9 +432,31 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
         // so the producer and the activation warp run out of time as well and
         // nothing more is copied into this CTA. Waits are voted warp-uniform.
         bool ok = true;
+        // Stage groups 1.. hand their partial sums of tile i to group 0 through
+        // `comb` (bounded waits on both sides); group 0 adds them in order.
+        auto combine = [&](int i) -> bool {
+            if constexpr (SG > 1) {
+                if (sg != 0) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_cempty, (i & 1) ^ 1, err))) return false;
+#pragma unroll
+                    for (int m = 0; m < ML; ++m) {
+                        comb[(m0 + m) * kGemvTileRows + r] = y[m];
+                        y[m] = 0.f;
+                    }
+                    mbar_arrive(bar_cfull);
+                } else {
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_cfull, i & 1, err))) return false;
+#pragma unroll
+                    for (int m = 0; m < ML; ++m) y[m] += comb[(m0 + m) * kGemvTileRows + r];
+                    mbar_arrive(bar_cempty);
+                }
+            }
+            return true;
+        };
         for (int i = 0; i < nt_local && ok; ++i) {
             for (int bl = 0; bl < nb; ++bl) {
                 const int st = i * nb + bl;
+                if (SG > 1 && st % SG != sg) continue;
                 const int s = st % S;
                 const uint32_t par = (st / S) & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_wfull + 8 * s, par, err) &&
@@ -449,7 +475,8 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             }
-            if (ok && C == 1) {  // C > 1: one tile per CTA, reduced across the cluster below
+            ok = ok && combine(i);
+            if (ok && C == 1 && sg == 0) {  // C > 1: one tile per CTA, reduced across the cluster below
                 const int t = cid + i * ncl;
                 const int mi = group_matrix(grp, t);
                 const int row = (t - grp.tile_start[mi]) * kGemvTileRows + r;
@@ -471,6 +498,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
             // in rank order. A rank that timed out pushes nothing; rank 0 always
             // waits (bounded) for the pushes before it exits, so none lands in the
             // shared memory of a CTA that has gone.
+            if (sg != 0) return;
             if (rank != 0) {
                 if (!ok) return;
                 const uint32_t dst = map_shared_rank(smem_u32(red + (rank - 1) * MT * kGemvTileRows), 0);
@@ -554,7 +582,8 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
                              const DeviceInfo& dev, int slot, int pdl, unsigned long long* amax) {
     const int KB = K / kBlockWeights;
     const int tiles = grp.tile_start[grp.count];
-    const int slots = dev.num_sms * dev.gemv_occ[XB ? 1 : 0][slot];
+    const int occ = dev.gemv_occ[XB ? 1 : 0][slot];
+    const int slots = dev.num_sms * (MT <= 2 && Q4K_GEMV_GRIDOCC > 0 && Q4K_GEMV_GRIDOCC < occ ? Q4K_GEMV_GRIDOCC : occ);
     int C = 1, kb_per = KB, grid;
     if (tiles >= slots) {
         // persistent, one CTA per resident slot (CTA c streams tiles c, c + grid,

@@ -19,6 +19,9 @@ struct DeviceInfo {
     // and resident clusters of C CTAs (index C, 2..16).
     int gemv_occ[2][5] = {};
     int gemv_clusters[2][5][17] = {};
+    // tensor-core decode kernel, same indexing (C up to 8)
+    int tc_occ[2][5] = {};
+    int tc_clusters[2][5][9] = {};
 };
 
 cudaError_t launch_dequant(const uint8_t* W, int64_t N, int64_t K, float* out, cudaStream_t stream,
@@ -52,6 +55,13 @@ __host__ __device__ inline int group_matrix(const WeightGroup& g, int t) {
 cudaError_t launch_gemv(const WeightGroup& grp, const void* X, bool x_bf16, int M, int K,
                         cudaStream_t stream, const DeviceInfo& dev, int pdl,
                         unsigned long long* amax = nullptr);
+// The same product on the tensor cores (1 <= M <= 16): the 4-bit codes are the
+// MMA's A operand and fp32 accuracy is kept by splitting X into bf16 hi + lo.
+cudaError_t launch_tcgemv(const WeightGroup& grp, const void* X, bool x_bf16, int M, int K,
+                          cudaStream_t stream, const DeviceInfo& dev, int pdl,
+                          unsigned long long* amax = nullptr);
+// Sets its attributes and fills dev.tc_occ / dev.tc_clusters.
+cudaError_t tcgemv_setup(DeviceInfo& dev);
 cudaError_t launch_argmax_init(unsigned long long* keys, int M, cudaStream_t stream);
 cudaError_t launch_argmax_finish(unsigned long long* keys, int M, cudaStream_t stream);
 // Sets the kernels' attributes and fills dev.gemv_occ / dev.gemv_clusters.
