@@ -42,7 +42,8 @@ if ROOT not in sys.path:
 
 METRIC = "Q4_K dequant-matmul: GEMV packed-weight GB/s (M=1); GEMM TFLOP/s (M=512)"
 DECODE_WL = 4                     # headline: the largest weight set, M = 1
-DECODE_EXTRA_WLS = (1, 2)         # keyed sub-results
+DECODE_EXTRA_WLS = (1, 2)         # keyed sub-results at M = 1
+DECODE_EXTRA_M = (4, 16)          # the headline weight set at more activation rows (tensor-core kernel)
 PREFILL_WL, PREFILL_M = 3, 512    # the GEMM metric
 GEMM_EXTRA = ((4, 2048), (3, 32), (3, 1024))
 LM_HEAD = (2, 128256, 3072)       # (workload, N, K) of the lm_head used by the argmax and dequant legs
@@ -519,7 +520,7 @@ def _sweep_record(torch, q4k, wl, mats, names, M, xdt, stream, steps, warmup, hb
     gbps = wbytes / (ms * 1e-3) / 1e9
     tf = flops / (ms * 1e-3) / 1e12
     rec = {"workload": synth.WORKLOADS[wl].name, "M": M, "x_dtype": xdt,
-           "kernel": "q4k_gemv_kernel" if M <= 16 else "q4k_gemm_kernel",
+           "kernel": ("q4k_gemv_kernel" if M <= 2 else "q4k_tcgemv_kernel") if M <= 16 else "q4k_gemm_kernel",
            "launches_per_step": len(calls), "steps": steps, "ms_per_step": round(ms, 5),
            "packed_GBps": round(gbps, 1), "frac_of_hbm": round(gbps / hbm, 4),
            "TFLOPs": round(tf, 2), "frac_of_bf16": round(tf / bf16_peak, 4)}
@@ -720,6 +721,14 @@ def run_gpu(args):
         del g4, calls4, calls4u
         torch.cuda.empty_cache()
 
+        # -------------------- the same weights at 4 and 16 activation rows ---
+        out["decode_rows"] = []
+        for M in DECODE_EXTRA_M:
+            rec, n = _sweep_record(torch, q4k, DECODE_WL, mats4, names4, M, "f32", stream, args.steps,
+                                   args.warmup, hbm, bf16_peak, barrier)
+            rec["kernel"] = "q4k_tcgemv_kernel"
+            launches += n
+            out["decode_rows"].append(rec)
         # ------------------------------------------- other decode sweeps ---
         out["decode_workloads"] = []
         for wl in DECODE_EXTRA_WLS:

@@ -4,9 +4,10 @@
 // Dispatch (the decode / prefill split of the rlx-llama32 page's "Decode" and
 // "Packed GGUF" sections):
 //   q4k_dequant              -> K1 q4k_dequant_kernel
-//   q4k_matmul      M <= 16  -> K2 q4k_gemv_kernel (fp32 activations)
-//                   M >  16  -> K2 over consecutive 16-row slices of X
-//   q4k_matmul_bf16 M <= 16  -> K2 q4k_gemv_kernel (bf16 activations)
+//   q4k_matmul      M <= 2   -> K2 q4k_gemv_kernel (CUDA cores, fp32 activations)
+//                   3..16    -> K4 q4k_tcgemv_kernel (tensor cores, fp32 accuracy)
+//                   M >  16  -> the same over consecutive 16-row slices of X
+//   q4k_matmul_bf16 M <= 16  -> K2 / K4 as above (bf16 activations)
 //                   M >= 17  -> K3 q4k_gemm_kernel (tcgen05, TMEM accumulators)
 //   q4k_matmul_multi[_bf16]  -> the same, for up to 8 matrices sharing K and X,
 //                   all of them in one launch (per 16-row slice for fp32 M > 16)
@@ -45,9 +46,12 @@ __global__ void q4k_selftest_timeout_kernel(unsigned long long limit_ns, unsigne
 namespace {
 
 // Decode products with at least this many activation rows (and at most 16)
-// run on the tensor cores (K4); fewer run on the CUDA cores (K2).
+// run on the tensor cores (K4), fewer on the CUDA cores (K2). K4's rate is
+// bound by the SM's MMA issue rate whatever M is; K2's falls with M. Measured
+// on the Qwen3-14B-shaped sweep: M = 1 K2 2.07 ms vs K4 3.3 ms; M = 4 K2 4.9
+// ms vs K4 4.25 ms; M = 16 K2 19.0 ms vs K4 6.2 ms.
 #ifndef Q4K_TC_MIN_M
-#define Q4K_TC_MIN_M 5
+#define Q4K_TC_MIN_M 3
 #endif
 
 cudaError_t launch_decode(const WeightGroup& grp, const void* X, bool xb, int M, int K, cudaStream_t stream,

@@ -53,19 +53,6 @@ constexpr int kGemvTileRows = 128;
 constexpr int kGemvConsumers = 4;  // consumer warps: one lane per row of the tile
 constexpr int kGemvStageBytes = kGemvTileRows * kBlockBytes;  // 18432
 
-#ifndef Q4K_GEMV_SGROUPS
-#define Q4K_GEMV_SGROUPS 2
-#endif
-#ifndef Q4K_GEMV_STAGES
-#define Q4K_GEMV_STAGES 4
-#endif
-#ifndef Q4K_GEMV_MINB
-#define Q4K_GEMV_MINB 2
-#endif
-#ifndef Q4K_GEMV_GRIDOCC
-#define Q4K_GEMV_GRIDOCC 0
-#endif
-
 template <int MT>
 struct GemvCfg {
     // M >= 8: two groups of consumer warps on the same rows and stages, each
@@ -76,7 +63,7 @@ struct GemvCfg {
     // M <= 2: kSGroups groups of consumer warps take alternate stages of the
     // same tile (more warps to hide latency); their partial sums are added at
     // the end of the tile, group 0 + group 1 (deterministic)
-    static constexpr int kSGroups = MT <= 2 ? Q4K_GEMV_SGROUPS : 1;
+    static constexpr int kSGroups = MT <= 2 ? 2 : 1;
     static constexpr int kStageConsumers = kGemvConsumers * kMGroups;  // warps reading a stage
     static constexpr int kConsumers = kStageConsumers * kSGroups;
     static constexpr int kProducerWarp = kConsumers;
@@ -85,8 +72,8 @@ struct GemvCfg {
     // registers: two resident CTAs per SM for small M (measured: more registers
     // per thread buy more overlap than a third CTA would); M >= 8 takes ~145-165
     // registers a thread at 320 threads, one CTA per SM
-    static constexpr int kMinBlocks = MT >= 8 ? 1 : (MT <= 2 ? Q4K_GEMV_MINB : 2);
-    static constexpr int kStages = MT <= 2 ? Q4K_GEMV_STAGES : 4;
+    static constexpr int kMinBlocks = MT >= 8 ? 1 : 2;
+    static constexpr int kStages = 4;
     static constexpr int kOffW = 0;
     static constexpr int kOffX = kOffW + kStages * kGemvStageBytes;     // x' [stage][m][256]
     static constexpr int kOffXs = kOffX + kStages * MT * 256 * 4;        // sums [stage][m][8]
@@ -582,8 +569,7 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
                              const DeviceInfo& dev, int slot, int pdl, unsigned long long* amax) {
     const int KB = K / kBlockWeights;
     const int tiles = grp.tile_start[grp.count];
-    const int occ = dev.gemv_occ[XB ? 1 : 0][slot];
-    const int slots = dev.num_sms * (MT <= 2 && Q4K_GEMV_GRIDOCC > 0 && Q4K_GEMV_GRIDOCC < occ ? Q4K_GEMV_GRIDOCC : occ);
+    const int slots = dev.num_sms * dev.gemv_occ[XB ? 1 : 0][slot];
     int C = 1, kb_per = KB, grid;
     if (tiles >= slots) {
         // persistent, one CTA per resident slot (CTA c streams tiles c, c + grid,

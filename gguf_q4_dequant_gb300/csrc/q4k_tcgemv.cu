@@ -40,37 +40,34 @@
 //
 // Warp roles (one CTA per SM):
 //   warp 0        TMA producer: one super-block of 128 rows per W stage
-//   warp 1        TMEM allocator and MMA issuer: per 64-k chunk 4 MMAs
-//                 (128 x N x 16) into the chunk's two sub-blocks' columns
-//   warps 2..9    expansion: thread = (row, half of the chunk's 32 code bytes):
-//                 reads the super-block's codes into registers, releases the W
-//                 stage, writes 32 bf16 operands per chunk into the swizzled
-//                 K-major A tile (and the row's 16-byte header for the readout)
-//   warps 10..13  readout (TMEM lane quadrant = warp % 4, lane = row): per
+//   warps 1..     MMA issuers (4, or 2 at M = 16; the first allocates TMEM):
+//                 per 64-k chunk 4 MMAs (128 x N x 16) into the chunk's two
+//                 sub-blocks' columns; issuer i takes the chunks c = i mod n,
+//                 so the waits and issue latencies of several chunks overlap
+//   8 warps       expansion: thread = (64-k chunk, rows r and r + 64): reads its
+//                 code bytes into registers, releases the W stage, writes 128
+//                 bf16 operands into the swizzled K-major A tile of the chunk
+//                 (chunk-0 threads also copy the rows' headers for the readout);
+//                 the four chunks of a super-block are expanded in parallel
+//   4 warps       readout (TMEM lane quadrant = warp % 4, lane = row): per
 //                 super-block, TMEM -> registers, scales, mins, and the
 //                 epilogue (Y stores, or the fused argmax keys)
-//   warps 14..    activations: per super-block, scale, split and write the
+//   last warps    activations: per super-block, scale, split and write the
 //                 B tiles, and the sub-block sums of x
-// Two TMEM buffers (super-block parity) let the MMAs of super-block b+1 run
-// while the readout drains b. All waits are bounded (see mbar_wait).
+// Two or four TMEM accumulator buffers (all 512 columns) let the MMAs of the
+// next super-blocks run while the readout drains one; the readout issues the
+// loads of several sub-blocks before one wait. All waits are bounded (see
+// mbar_wait).
 #include "q4k_device.cuh"
 #include "q4k_internal.h"
 
 namespace q4k {
 
-// Operand encoding of the codes: 0 -> subnormal bf16 q * 2^-133 (one AND per
-// pair); 1 -> normal bf16 128 + q (an OR with 0x4300 per pair, and the offset
-// 128 * sum(x) removed in the readout).
-#ifndef Q4K_TC_MAGIC
-#define Q4K_TC_MAGIC 0
-#endif
-constexpr bool kTcMagic = Q4K_TC_MAGIC != 0;
-
 constexpr int kTcRows = 128;
 constexpr int kTcWStageBytes = kTcRows * kBlockBytes;  // 18432
 constexpr int kTcAStepBytes = kTcRows * 128;           // 128 rows x 64 k bf16 (one 64-k chunk)
-constexpr int kTcExpThreads = 256;                     // warps 2..9
-constexpr int kTcReadThreads = 128;                    // warps 10..13
+constexpr int kTcExpThreads = 256;                     // 8 expansion warps
+constexpr int kTcReadThreads = 128;                    // 4 readout warps
 
 template <int MT>
 struct TcCfg {
@@ -80,23 +77,37 @@ struct TcCfg {
     static constexpr int kXWarps = MT >= 8 ? MT / 4 : 1;    // activation warps
     static constexpr int kXRows = MT / kXWarps;              // activation rows per warp
     static constexpr int kWS = 4;                            // W ring (super-blocks)
-    static constexpr int kAS = 4;                            // chunk ring (A + B tiles)
+    static constexpr int kBS = kN == 16 ? 12 : 8;            // B tile ring (chunks): the activation
+                                                             // warps run up to 2-3 super-blocks ahead
     static constexpr int kHR = 4;                            // per-super-block side data ring
     static constexpr int kMaxSplit = MT >= 16 ? 4 : 8;
-    static constexpr int kWarpX = 14;
+    static constexpr int kAS = 4;                            // A tile ring (chunks: one super-block)
+    // MMA-issuing warps: warp i of them takes chunk c of every super-block with
+    // c % kMmaWarps == i, so their barrier waits and issue latencies overlap
+    // (measured: one warp 122 us, two 82 us, four 83 us on a 128256 x 3072
+    // matrix at M = 1 -- beyond two, the SM's MMA issue rate is the limit)
+    static constexpr int kMmaWarps = 2;
+    static constexpr int kWarpMma = 1;
+    static constexpr int kWarpExp = kWarpMma + kMmaWarps;
+    static constexpr int kWarpRead = kWarpExp + 8;
+    static constexpr int kWarpX = kWarpRead + 4;
     static constexpr int kThreads = 32 * (kWarpX + kXWarps);
-    static constexpr uint32_t kTmemCols = 2 * 8 * kN;        // 2 buffers x 8 sub-blocks x N
+    static constexpr int kNAcc = 512 / (8 * kN);             // accumulator buffers (4 or 2)
+    static constexpr uint32_t kTmemCols = kNAcc * 8 * kN;    // all 512 columns
+    static constexpr int kCPJ = 2 * kMH;                     // TMEM columns per sub-block and pass
+    static constexpr int kJB = kCPJ <= 4 ? 8 : (kCPJ <= 8 ? 4 : (MT >= 16 ? 1 : 2));  // sub-blocks per TMEM wait
     static constexpr int kBStepBytes = kN * 128;
     static constexpr int kOffA = 0;                                            // 1024-aligned
     static constexpr int kOffB = kOffA + kAS * kTcAStepBytes;                  // 1024-aligned
-    static constexpr int kOffW = kOffB + kAS * kBStepBytes;
+    static constexpr int kOffW = kOffB + kBS * kBStepBytes;
     static constexpr int kOffHdr = kOffW + kWS * kTcWStageBytes;               // [HR][128] x 16 B
     static constexpr int kOffXs = kOffHdr + kHR * kTcRows * 16;                // [HR][MT][8] sum_k x
     static constexpr int kOffG = kOffXs + kHR * MT * 8 * 4;                    // [HR][MT][2] 2^(133-S)
     static constexpr int kOffRed = kOffG + kHR * MT * 2 * 4;                   // [kMaxSplit-1][MT][128]
     static constexpr int kOffBar = kOffRed + (kMaxSplit - 1) * MT * kTcRows * 4;
-    // wfull[WS] wempty[WS] sfull[AS] sempty[AS] hfull[HR] hempty[HR] accfull[2] accempty[2] red fin
-    static constexpr int kNumBars = 2 * kWS + 2 * kAS + 2 * kHR + 4 + 2;
+    // wfull[WS] wempty[WS] afull[AS] aempty[AS] bfull[BS] bempty[BS] hfull[HR] hempty[HR]
+    // accfull[4] accempty[4] red fin
+    static constexpr int kNumBars = 2 * kWS + 2 * kAS + 2 * kBS + 2 * kHR + 8 + 2;
     static constexpr int kOffTmem = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffTmem + 16 + 1024;  // + alignment slack
     static_assert(kSmem <= 232448, "shared memory");
@@ -119,7 +130,7 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
     q4k_tcgemv_kernel(const __grid_constant__ WeightGroup grp, const void* __restrict__ X, int M, int K,
                       int C, int kb_per, int pdl_flags, unsigned long long* amax, unsigned int* err) {
     using Cfg = TcCfg<MT>;
-    constexpr int WS = Cfg::kWS, AS = Cfg::kAS, HR = Cfg::kHR, N = Cfg::kN;
+    constexpr int WS = Cfg::kWS, AS = Cfg::kAS, BS = Cfg::kBS, HR = Cfg::kHR, N = Cfg::kN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -139,13 +150,15 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
 
     const uint32_t b_wfull = sbase + Cfg::kOffBar;
     const uint32_t b_wempty = b_wfull + 8 * WS;
-    const uint32_t b_sfull = b_wempty + 8 * WS;
-    const uint32_t b_sempty = b_sfull + 8 * AS;
-    const uint32_t b_hfull = b_sempty + 8 * AS;
+    const uint32_t b_afull = b_wempty + 8 * WS;
+    const uint32_t b_aempty = b_afull + 8 * AS;
+    const uint32_t b_bfull = b_aempty + 8 * AS;
+    const uint32_t b_bempty = b_bfull + 8 * BS;
+    const uint32_t b_hfull = b_bempty + 8 * BS;
     const uint32_t b_hempty = b_hfull + 8 * HR;
     const uint32_t b_accfull = b_hempty + 8 * HR;
-    const uint32_t b_accempty = b_accfull + 16;
-    const uint32_t b_red = b_accempty + 16;
+    const uint32_t b_accempty = b_accfull + 32;
+    const uint32_t b_red = b_accempty + 32;
     const uint32_t b_fin = b_red + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmem);
     float* red = reinterpret_cast<float*>(smem + Cfg::kOffRed);
@@ -156,23 +169,27 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
             mbar_init(b_wempty + 8 * i, kTcExpThreads);    // every expansion thread
         }
         for (int i = 0; i < AS; ++i) {
-            mbar_init(b_sfull + 8 * i, kTcExpThreads + 32 * Cfg::kXWarps);  // A and B tile writers
-            mbar_init(b_sempty + 8 * i, 1);                // the MMA commit
+            mbar_init(b_afull + 8 * i, kTcExpThreads / 4);  // the expansion threads of one chunk
+            mbar_init(b_aempty + 8 * i, 1);                // the MMA commit
+        }
+        for (int i = 0; i < BS; ++i) {
+            mbar_init(b_bfull + 8 * i, 32 * Cfg::kXWarps);  // the activation lanes
+            mbar_init(b_bempty + 8 * i, 1);                 // the MMA commit
         }
         for (int i = 0; i < HR; ++i) {
-            mbar_init(b_hfull + 8 * i, kTcRows + 32 * Cfg::kXWarps);  // headers + activation sums
+            mbar_init(b_hfull + 8 * i, kTcExpThreads / 4 + 32 * Cfg::kXWarps);  // headers + activation sums
             mbar_init(b_hempty + 8 * i, kTcReadThreads);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(b_accfull + 8 * i, 1);               // the MMA commit
+        for (int i = 0; i < Cfg::kNAcc; ++i) {
+            mbar_init(b_accfull + 8 * i, Cfg::kMmaWarps);  // one commit per MMA warp
             mbar_init(b_accempty + 8 * i, kTcReadThreads);
         }
         mbar_init(b_red, 1);
-        mbar_init(b_fin, 1);
+        mbar_init(b_fin, Cfg::kMmaWarps);
         fence_barrier_init();
         if (C > 1 && rank == 0) mbar_arrive_expect_tx(b_red, (C - 1) * MT * kTcRows * 4);
     }
-    if (warp == 1) {
+    if (warp == Cfg::kWarpMma) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
         tmem_relinquish();
     }
@@ -206,24 +223,27 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                 mbar_wait(b_wfull + 8 * (sb % WS), (sb / WS) & 1, err, kDrainLimitNs);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer ---
+    } else if (warp < Cfg::kWarpExp) {
+        // ----------------------------------------------------- MMA issuers ---
         constexpr uint32_t idesc = idesc_bf16_f32(kTcRows, N);
+        constexpr int NA = Cfg::kNAcc, MW = Cfg::kMmaWarps;
+        const int mw = warp - Cfg::kWarpMma;
         for (int sb = 0; sb < total; ++sb) {
-            const int u = sb & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(b_accempty + 8 * u, ((sb >> 1) & 1) ^ 1, err))) break;
+            const int u = sb % NA;
+            if (!__all_sync(0xffffffffu, mbar_wait(b_accempty + 8 * u, ((sb / NA) & 1) ^ 1, err))) break;
             tc_fence_after();
             bool ok = true;
-            for (int c = 0; c < 4; ++c) {
-                const int st = 4 * sb + c, as = st % AS;
-                if (!__all_sync(0xffffffffu, mbar_wait(b_sfull + 8 * as, (st / AS) & 1, err))) {
+            for (int c = mw; c < 4; c += MW) {
+                const int st = 4 * sb + c, as = st % AS, bs = st % BS;
+                if (!__all_sync(0xffffffffu, mbar_wait(b_bfull + 8 * bs, (st / BS) & 1, err) &&
+                                                 mbar_wait(b_afull + 8 * as, (st / AS) & 1, err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (elect_one()) {
                     const uint64_t a0 = sw128_desc(sbase + Cfg::kOffA + as * kTcAStepBytes);
-                    const uint64_t b0 = sw128_desc(sbase + Cfg::kOffB + as * Cfg::kBStepBytes);
+                    const uint64_t b0 = sw128_desc(sbase + Cfg::kOffB + bs * Cfg::kBStepBytes);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         // chunk c holds sub-blocks 2c (k 0..31) and 2c+1 (k 32..63); the
@@ -231,7 +251,8 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                         const uint32_t d = tmem + static_cast<uint32_t>((u * 8 + 2 * c + (kk >> 1)) * N);
                         tc_mma_bf16(d, a0 + 2 * kk, b0 + 2 * kk, idesc, kk & 1);
                     }
-                    tc_commit(b_sempty + 8 * as);
+                    tc_commit(b_aempty + 8 * as);
+                    tc_commit(b_bempty + 8 * bs);
                 }
                 __syncwarp();
             }
@@ -241,64 +262,65 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
         }
         if (elect_one()) tc_commit(b_fin);  // every MMA of this thread has completed
         __syncwarp();
-    } else if (warp < 10) {
+    } else if (warp < Cfg::kWarpRead) {
         // ------------------------------------------------------- expansion ---
-        const int t = threadIdx.x - 64;
-        const int r = t & (kTcRows - 1);   // weight row
-        const int h = t >> 7;              // which 16 of each chunk's 32 code bytes (warp-uniform)
+        // thread = (chunk c of the super-block, rows r0 and r0 + 64): one step
+        // per super-block, the four chunks in parallel
+        const int t = threadIdx.x - 32 * Cfg::kWarpExp;
+        const int c = t >> 6;              // warp-uniform (two warps per chunk)
+        const int r0 = t & 63;
         for (int sb = 0; sb < total; ++sb) {
             const int ws = sb % WS;
             if (!mbar_wait(b_wfull + 8 * ws, (sb / WS) & 1, err)) break;
-            const uint8_t* P = smem + Cfg::kOffW + ws * kTcWStageBytes + r * kBlockBytes;
-            uint4 q[4];
+            uint4 q[2][2], hd[2];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) q[c] = *reinterpret_cast<const uint4*>(P + 16 + 32 * c + 16 * h);
-            uint4 hd = make_uint4(0u, 0u, 0u, 0u);
-            if (h == 0) hd = *reinterpret_cast<const uint4*>(P);
+            for (int rr = 0; rr < 2; ++rr) {
+                const uint8_t* P = smem + Cfg::kOffW + ws * kTcWStageBytes + (r0 + 64 * rr) * kBlockBytes;
+                q[rr][0] = *reinterpret_cast<const uint4*>(P + 16 + 32 * c);
+                q[rr][1] = *reinterpret_cast<const uint4*>(P + 32 + 32 * c);
+                hd[rr] = c == 0 ? *reinterpret_cast<const uint4*>(P) : make_uint4(0u, 0u, 0u, 0u);
+            }
             mbar_arrive(b_wempty + 8 * ws);
-            if (h == 0) {
+            if (c == 0) {  // the rows' headers, for the readout
                 const int hs = sb % HR;
                 if (!mbar_wait(b_hempty + 8 * hs, ((sb / HR) & 1) ^ 1, err)) break;
-                *reinterpret_cast<uint4*>(smem + Cfg::kOffHdr + (hs * kTcRows + r) * 16) = hd;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr)
+                    *reinterpret_cast<uint4*>(smem + Cfg::kOffHdr + (hs * kTcRows + r0 + 64 * rr) * 16) = hd[rr];
                 mbar_arrive(b_hfull + 8 * hs);
             }
-            bool ok = true;
+            // word i of the chunk row (bytes 4i..4i+3): low nibbles are k = 4i..4i+3
+            // (positions 4i.. in the order 0, 2, 1, 3), high nibbles k = 32 + 4i..
+            uint32_t lo[2][16], hi[2][16];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int st = 4 * sb + c, as = st % AS;
-                const uint32_t w[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
-                uint32_t lo[8], hi[8];
+            for (int rr = 0; rr < 2; ++rr) {
+                const uint32_t w[8] = {q[rr][0].x, q[rr][0].y, q[rr][0].z, q[rr][0].w,
+                                       q[rr][1].x, q[rr][1].y, q[rr][1].z, q[rr][1].w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const uint32_t v8 = w[i] >> 8;
-                    if constexpr (kTcMagic) {
-                        lo[2 * i] = (w[i] & 0x000F000Fu) | 0x43004300u;
-                        lo[2 * i + 1] = (v8 & 0x000F000Fu) | 0x43004300u;
-                        hi[2 * i] = ((w[i] >> 4) & 0x000F000Fu) | 0x43004300u;
-                        hi[2 * i + 1] = ((w[i] >> 12) & 0x000F000Fu) | 0x43004300u;
-                    } else {
-                        lo[2 * i] = w[i] & 0x000F000Fu;      // k 4i+0, 4i+2 (low nibbles of bytes 0, 2)
-                        lo[2 * i + 1] = v8 & 0x000F000Fu;    // k 4i+1, 4i+3 (bytes 1, 3)
-                        hi[2 * i] = w[i] & 0x00F000F0u;      // high nibbles, 16q
-                        hi[2 * i + 1] = v8 & 0x00F000F0u;
-                    }
+                    lo[rr][2 * i] = w[i] & 0x000F000Fu;      // k 4i+0, 4i+2 (low nibbles of bytes 0, 2)
+                    lo[rr][2 * i + 1] = v8 & 0x000F000Fu;    // k 4i+1, 4i+3 (bytes 1, 3)
+                    hi[rr][2 * i] = w[i] & 0x00F000F0u;      // high nibbles, 16q
+                    hi[rr][2 * i + 1] = v8 & 0x00F000F0u;
                 }
-                if (!mbar_wait(b_sempty + 8 * as, ((st / AS) & 1) ^ 1, err)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* arow = smem + Cfg::kOffA + as * kTcAStepBytes + r * 128;
-                const int sw = r & 7;
-                // low nibbles: positions 16h .. 16h+15 (16-byte chunks 2h, 2h+1);
-                // high nibbles: 32 + 16h .. (chunks 4+2h, 5+2h)
-                *reinterpret_cast<uint4*>(arow + (((2 * h) ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                *reinterpret_cast<uint4*>(arow + (((2 * h + 1) ^ sw) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-                *reinterpret_cast<uint4*>(arow + (((4 + 2 * h) ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(arow + (((5 + 2 * h) ^ sw) << 4)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-                fence_proxy_async_smem();
-                mbar_arrive(b_sfull + 8 * as);
             }
-            if (!ok) break;
+            const int st = 4 * sb + c, as = st % AS;
+            if (!mbar_wait(b_aempty + 8 * as, ((st / AS) & 1) ^ 1, err)) break;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = r0 + 64 * rr, sw = r & 7;
+                uint8_t* arow = smem + Cfg::kOffA + as * kTcAStepBytes + r * 128;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte chunks q4 (low) and 4 + q4 (high)
+                    *reinterpret_cast<uint4*>(arow + ((q4 ^ sw) << 4)) =
+                        make_uint4(lo[rr][4 * q4], lo[rr][4 * q4 + 1], lo[rr][4 * q4 + 2], lo[rr][4 * q4 + 3]);
+                    *reinterpret_cast<uint4*>(arow + (((4 + q4) ^ sw) << 4)) =
+                        make_uint4(hi[rr][4 * q4], hi[rr][4 * q4 + 1], hi[rr][4 * q4 + 2], hi[rr][4 * q4 + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(b_afull + 8 * as);
         }
     } else if (warp < Cfg::kWarpX) {
         // --------------------------------------------------------- readout ---
@@ -313,9 +335,9 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
         bool ok = true;
         for (int i = 0; i < nt_local && ok; ++i) {
             for (int bl = 0; bl < nb; ++bl) {
-                const int sb = i * nb + bl, u = sb & 1, hs = sb % HR;
+                const int sb = i * nb + bl, u = sb % Cfg::kNAcc, hs = sb % HR;
                 if (!__all_sync(0xffffffffu, mbar_wait(b_hfull + 8 * hs, (sb / HR) & 1, err) &&
-                                                 mbar_wait(b_accfull + 8 * u, (sb >> 1) & 1, err))) {
+                                                 mbar_wait(b_accfull + 8 * u, (sb / Cfg::kNAcc) & 1, err))) {
                     ok = false;
                     break;
                 }
@@ -331,42 +353,36 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                     float qa[MH], ma[MH];
 #pragma unroll
                     for (int m = 0; m < MH; ++m) qa[m] = ma[m] = 0.f;
+                    constexpr int JB = Cfg::kJB;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint32_t v[2 * MH];
-                        tmem_ld_32x32b(tl + static_cast<uint32_t>((u * 8 + j) * N + 2 * p0), v);
-                        tmem_ld_wait();
+                    for (int j0 = 0; j0 < 8; j0 += JB) {
+                    // JB sub-blocks' loads in flight together, one wait
+                    uint32_t vb[JB][2 * MH];
+#pragma unroll
+                    for (int jj = 0; jj < JB; ++jj)
+                        tmem_ld_32x32b(tl + static_cast<uint32_t>((u * 8 + j0 + jj) * N + 2 * p0), vb[jj]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < JB; ++jj) {
+                        const int j = j0 + jj;
+                        const uint32_t (&v)[2 * MH] = vb[jj];
                         const uint32_t scw = j < 4 ? scb.sc_lo : scb.sc_hi;
                         const uint32_t mw = j < 4 ? scb.m_lo : scb.m_hi;
                         const float mj = byte_to_float(mw, j & 3);
-                        if constexpr (kTcMagic) {
-                            // D_j = 128 * sum x' + sum q x' (x' = hi + lo, scaled)
-                            const float scj = byte_to_float(scw, j & 3);
-                            const float cj = fmaf(128.f * d, scj, dmin * mj);
+                        // high-nibble sub-blocks (odd j) carry 16q: sc/16 is exact
+                        const float scj = byte_to_float(scw, j & 3) * ((j & 1) ? 0.0625f : 1.f);
 #pragma unroll
-                            for (int m = 0; m < MH; ++m) {
-                                const float sj = __uint_as_float(v[2 * m]) + __uint_as_float(v[2 * m + 1]);
-                                qa[m] = fmaf(scj, sj, qa[m]);
-                                ma[m] = fmaf(cj, xsum[(p0 + m) * 8 + j], ma[m]);
-                            }
-                        } else {
-                            // high-nibble sub-blocks (odd j) carry 16q: sc/16 is exact
-                            const float scj = byte_to_float(scw, j & 3) * ((j & 1) ? 0.0625f : 1.f);
-#pragma unroll
-                            for (int m = 0; m < MH; ++m) {
-                                const float sj = __uint_as_float(v[2 * m]) + __uint_as_float(v[2 * m + 1]);
-                                qa[m] = fmaf(scj, sj, qa[m]);
-                                ma[m] = fmaf(mj, xsum[(p0 + m) * 8 + j], ma[m]);
-                            }
+                        for (int m = 0; m < MH; ++m) {
+                            const float sj = __uint_as_float(v[2 * m]) + __uint_as_float(v[2 * m + 1]);
+                            qa[m] = fmaf(scj, sj, qa[m]);
+                            ma[m] = fmaf(mj, xsum[(p0 + m) * 8 + j], ma[m]);
                         }
+                    }
                     }
 #pragma unroll
                     for (int m = 0; m < MH; ++m) {
                         const float g1 = gf[2 * (p0 + m)], g2 = gf[2 * (p0 + m) + 1];
-                        if constexpr (kTcMagic)  // the scaled sums and the q-term share the scale 2^-S
-                            y[p0 + m] += ((d * qa[m] - ma[m]) * g1) * g2;
-                        else
-                            y[p0 + m] += d * ((qa[m] * g1) * g2) - dmin * ma[m];
+                        y[p0 + m] += d * ((qa[m] * g1) * g2) - dmin * ma[m];
                     }
                 }
                 tc_fence_before();
@@ -465,10 +481,10 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int st = 4 * sb + cc;
-                ok = ok && mbar_wait(b_sempty + 8 * (st % AS), ((st / AS) & 1) ^ 1, err);
+                ok = ok && mbar_wait(b_bempty + 8 * (st % BS), ((st / BS) & 1) ^ 1, err);
             }
             if (!__all_sync(0xffffffffu, ok)) break;
-            uint8_t* bt = smem + Cfg::kOffB + ((4 * sb + c) % AS) * Cfg::kBStepBytes;
+            uint8_t* bt = smem + Cfg::kOffB + ((4 * sb + c) % BS) * Cfg::kBStepBytes;
             float* xsum = reinterpret_cast<float*>(smem + Cfg::kOffXs) + hs * MT * 8;
             float* gf = reinterpret_cast<float*>(smem + Cfg::kOffG) + hs * MT * 2;
 #pragma unroll
@@ -484,15 +500,13 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                 amax_bits = __reduce_max_sync(0xffffffffu, amax_bits);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 1);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                // S: the block's largest |x| to [2^120, 2^121) (subnormal codes; 133 - S
-                // back in the readout) or to [1, 2) (codes 128 + q; -S back)
+                // S: the block's largest |x| to [2^120, 2^121); 133 - S back in the readout
                 int e = static_cast<int>(amax_bits >> 23) - 127;
                 e = e < -126 ? -126 : e;
-                const int S = (kTcMagic ? 0 : 120) - e;
+                const int S = 120 - e;
                 float s1, s2, g1, g2;
                 exp2_pair(S, s1, s2);
-                exp2_pair((kTcMagic ? 0 : 133) - S, g1, g2);
-                float ssum = 0.f;  // the scaled sums hi + lo the MMA saw (codes 128 + q)
+                exp2_pair(133 - S, g1, g2);
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
@@ -504,15 +518,6 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                     const __nv_bfloat162 ll = __floats2bfloat162_rn(xa - hf.x, xb - hf.y);
                     hw[p] = *reinterpret_cast<const uint32_t*>(&hh);
                     lw[p] = *reinterpret_cast<const uint32_t*>(&ll);
-                    if constexpr (kTcMagic) {
-                        const float2 lf = __bfloat1622float2(ll);
-                        ssum += (hf.x + lf.x) + (hf.y + lf.y);
-                    }
-                }
-                if constexpr (kTcMagic) {
-                    ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
-                    ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
-                    sum = ssum;
                 }
                 *reinterpret_cast<uint4*>(bt + sw128_offset(2 * mm, lane & 7)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(bt + sw128_offset(2 * mm + 1, lane & 7)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -524,14 +529,14 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
             }
             fence_proxy_async_smem();
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) mbar_arrive(b_sfull + 8 * ((4 * sb + cc) % AS));
+            for (int cc = 0; cc < 4; ++cc) mbar_arrive(b_bfull + 8 * ((4 * sb + cc) % BS));
             mbar_arrive(b_hfull + 8 * hs);
         }
     }
-    if (C > 1 && !(warp >= 10 && warp < Cfg::kWarpX)) cluster_wait();  // every thread that arrived waits once
+    if (C > 1 && !(warp >= Cfg::kWarpRead && warp < Cfg::kWarpX)) cluster_wait();  // each arrival waits once
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == Cfg::kWarpMma) {
         mbar_wait(b_fin, 0, err);
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
