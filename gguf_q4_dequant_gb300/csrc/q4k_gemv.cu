@@ -579,8 +579,12 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
         grid = slots;
     } else {
         // split K across a cluster (at least one super-block per CTA), as wide
-        // as the CTA slots allow while every cluster is resident at once
-        int c = slots / tiles;
+        // as four fifths of the CTA slots allow while every cluster is
+        // resident at once. Leaving a fifth free lets the next launch's
+        // clusters start (and stream their weights) before this launch ends;
+        // measured on a 7168 x 5120 grouped q/k/v launch: 280 CTAs 10.2 us,
+        // 224 CTAs 6.9 us.
+        int c = (4 * slots / 5) / tiles;
         c = c > GemvCfg<MT>::kMaxSplit ? GemvCfg<MT>::kMaxSplit : c;
         c = c > KB ? KB : c;
         C = 1;
