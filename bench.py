@@ -582,6 +582,31 @@ def _dequant_leg(torch, q4k, dev, stream, steps, warmup, hbm, barrier=lambda: No
     return rec, steps
 
 
+def run_sweep_only(args):
+    """Profiling aid: only the headline decode sweep (weights, the grouped calls,
+    one CUDA graph, timing); `--only dequant`: only the standalone dequant leg."""
+    torch, q4k, dev = _gpu_setup(args)
+    stream = torch.cuda.Stream()
+    hbm, _, _, _ = _peaks()
+    if args.only == "dequant":
+        rec, _ = _dequant_leg(torch, q4k, dev, stream, args.steps, args.warmup, hbm)
+        rec["device_error"] = q4k.q4k_device_error()
+        print(json.dumps(rec))
+        return
+    from gguf_q4_dequant_gb300 import synth
+    w, mats, names = _weights(DECODE_WL, dev, args.layers, with_names=True)
+    xs = {K: synth.activations(synth.x_seed(DECODE_WL, K, 1), 1, K).to(dev)
+          for K in sorted({K for (_, _, K) in mats})}
+    y = torch.empty(sum(N for (_, N, _) in mats), device=dev)
+    calls = _grouped_calls(q4k, mats, names, xs, y, stream.cuda_stream)
+    g = _capture(torch, calls, stream)
+    ms = _time_graph(torch, g, stream, args.steps, args.warmup, lambda: None)
+    wb = sum(Wd.numel() for (Wd, _, _) in mats)
+    print(json.dumps({"workload": w.name, "layers": args.layers or w.layers, "launches_per_step": len(calls),
+                      "ms_per_step": round(ms, 5), "packed_GBps": round(wb / ms / 1e6, 1),
+                      "frac_of_hbm": round(wb / ms / 1e6 / hbm, 4), "device_error": q4k.q4k_device_error()}))
+
+
 def run_gpu(args):
     import torch
     ws, rank, local = _dist()
@@ -910,8 +935,9 @@ def main():
     ap.add_argument("--dequant-sample", default="", help="(internal) rows saved by the GPU run")
     ap.add_argument("--pdl", type=int, default=2, choices=[0, 1, 2],
                     help="q4k_set_pdl mode for the sweeps (2: weights may stream early)")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill"],
-                    help="profiling aid: run one leg only")
+    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill", "sweep", "dequant"],
+                    help="profiling aid: run one leg only (sweep: the headline decode sweep alone; "
+                         "dequant: the standalone dequant leg alone)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: use only the first L layers of each weight set")
     ap.add_argument("--profile-shape", default="",
@@ -935,6 +961,8 @@ def main():
         run_profile_shape(args)
     elif args.all_configs:
         run_all_configs(args)
+    elif args.only in ("sweep", "dequant"):
+        run_sweep_only(args)
     else:
         run_gpu(args)
 
