@@ -11,7 +11,7 @@
 //                   M >= 17  -> K3 q4k_gemm_kernel (tcgen05, TMEM accumulators)
 //   q4k_matmul_multi[_bf16]  -> the same, for up to 8 matrices sharing K and X,
 //                   all of them in one launch (per 16-row slice for fp32 M > 16)
-//   q4k_matmul_argmax[_bf16] -> K2 with the fused argmax epilogue (M <= 16)
+//   q4k_matmul_argmax[_bf16] -> K2 / K4 with the fused argmax epilogue (M <= 16)
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -59,6 +59,16 @@ cudaError_t launch_decode(const WeightGroup& grp, const void* X, bool xb, int M,
     if (M >= Q4K_TC_MIN_M) return launch_tcgemv(grp, X, xb, M, K, stream, dev, pdl, amax);
     return launch_gemv(grp, X, xb, M, K, stream, dev, pdl, amax);
 }
+
+// bf16 activations with at most this many rows run the decode kernels; more
+// rows run the tcgen05 GEMM. (A 32-row variant of the tensor-core decode
+// kernel was measured at 240 us per Qwen3-8B-shaped layer of 32 rows against
+// the GEMM's 87 us: with 32 columns its readout of 8 sub-blocks x 32 rows per
+// super-block outweighs the MMAs, so 17.. rows stay on the GEMM.)
+#ifndef Q4K_DECODE_MAX_BF16
+#define Q4K_DECODE_MAX_BF16 16
+#endif
+constexpr int64_t kDecodeMaxBf16 = Q4K_DECODE_MAX_BF16;
 
 constexpr int kMaxDevices = 64;
 
@@ -236,7 +246,7 @@ int make_group(WeightGroup* grp, int count, const void* const* W, const int64_t*
     return Q4K_OK;
 }
 
-// One GEMV launch per 16-row slice of X over `count` matrices sharing K and X.
+// One decode launch per 16-row slice of X over `count` matrices sharing K and X.
 int run_gemv(int count, const void* const* W, const int64_t* N, int64_t K, const void* X, bool xb,
              int64_t M, float* const* Y, cudaStream_t stream, const DeviceInfo& dev) {
     WeightGroup grp;
@@ -377,7 +387,7 @@ int q4k_matmul_bf16(const void* W, int64_t N, int64_t K, const uint16_t* X_bf16,
     const DeviceInfo* dev = nullptr;
     if ((rc = current_device(&dev)) != Q4K_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M <= 16) return run_gemv(1, &W, &N, K, X_bf16, true, M, &Y, st, *dev);
+    if (M <= kDecodeMaxBf16) return run_gemv(1, &W, &N, K, X_bf16, true, M, &Y, st, *dev);
     return run_gemm(1, &W, &N, K, X_bf16, M, &Y, st, *dev);
 }
 
@@ -397,7 +407,7 @@ int q4k_matmul_multi_bf16(int count, const void* const* W, const int64_t* N, int
     const DeviceInfo* dev = nullptr;
     if ((rc = current_device(&dev)) != Q4K_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M <= 16) return run_gemv(count, W, N, K, X_bf16, true, M, Y, st, *dev);
+    if (M <= kDecodeMaxBf16) return run_gemv(count, W, N, K, X_bf16, true, M, Y, st, *dev);
     return run_gemm(count, W, N, K, X_bf16, M, Y, st, *dev);
 }
 

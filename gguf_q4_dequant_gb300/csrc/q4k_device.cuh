@@ -258,7 +258,10 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)
         : "r"(taddr)
         : "memory");
 }
-// 32 lanes x N consecutive 32-bit columns (N = 2, 4, 8, 16) from TMEM into registers.
+// 32 lanes x N consecutive 32-bit columns (N = 1, 2, 4, 8, 16) from TMEM into registers.
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&v)[1]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v[0]) : "r"(taddr) : "memory");
+}
 __device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&v)[2]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
                  : "=r"(v[0]), "=r"(v[1])

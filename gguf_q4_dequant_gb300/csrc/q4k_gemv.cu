@@ -579,12 +579,13 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
         grid = slots;
     } else {
         // split K across a cluster (at least one super-block per CTA), as wide
-        // as four fifths of the CTA slots allow while every cluster is
-        // resident at once. Leaving a fifth free lets the next launch's
-        // clusters start (and stream their weights) before this launch ends;
-        // measured on a 7168 x 5120 grouped q/k/v launch: 280 CTAs 10.2 us,
-        // 224 CTAs 6.9 us.
-        int c = (4 * slots / 5) / tiles;
+        // as 85 % of the CTA slots allow while every cluster is resident at
+        // once. The free slots let the next launch's clusters start (and
+        // stream their weights) before this launch ends. Measured per launch
+        // (304 slots): 7168 x 5120 q/k/v 280 CTAs 10.2 us, 224 CTAs 6.9 us;
+        // 5120 x 17408 down 280 CTAs 16.9 us, 240 CTAs 14.1 us; 16384 x 2048
+        // gate/up 256 CTAs 6.35 us, 128 CTAs 9.5 us.
+        int c = (17 * slots / 20) / tiles;
         c = c > GemvCfg<MT>::kMaxSplit ? GemvCfg<MT>::kMaxSplit : c;
         c = c > KB ? KB : c;
         C = 1;

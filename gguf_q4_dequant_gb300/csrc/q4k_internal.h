@@ -56,7 +56,7 @@ cudaError_t launch_gemv(const WeightGroup& grp, const void* X, bool x_bf16, int 
                         cudaStream_t stream, const DeviceInfo& dev, int pdl,
                         unsigned long long* amax = nullptr);
 // The same product on the tensor cores (1 <= M <= 16): the 4-bit codes are the
-// MMA's A operand and fp32 accuracy is kept by splitting X into bf16 hi + lo.
+// MMA's A operand; fp32 X is split into bf16 hi + lo to keep fp32 accuracy.
 cudaError_t launch_tcgemv(const WeightGroup& grp, const void* X, bool x_bf16, int M, int K,
                           cudaStream_t stream, const DeviceInfo& dev, int pdl,
                           unsigned long long* amax = nullptr);

@@ -69,9 +69,13 @@ constexpr int kTcAStepBytes = kTcRows * 128;           // 128 rows x 64 k bf16 (
 constexpr int kTcExpThreads = 256;                     // 8 expansion warps
 constexpr int kTcReadThreads = 128;                    // 4 readout warps
 
-template <int MT>
+template <int MT, bool XB>
 struct TcCfg {
-    static constexpr int kCols = 2 * MT;                     // x_hi(m), x_lo(m) at 2m, 2m+1
+    // fp32 activations: columns 2m (hi) and 2m+1 (lo); bf16 activations are
+    // exact in bf16 (and stay so scaled by 2^S), so column m holds x' alone
+    static constexpr bool kLo = !XB;
+    static constexpr int kCPM = kLo ? 2 : 1;                 // B columns per activation row
+    static constexpr int kCols = kCPM * MT;
     static constexpr int kMH = MT < 8 ? MT : 8;              // activation rows per readout pass
     static constexpr int kN = kCols <= 16 ? 16 : 32;         // MMA N
     static constexpr int kXWarps = MT >= 8 ? MT / 4 : 1;    // activation warps
@@ -94,7 +98,7 @@ struct TcCfg {
     static constexpr int kThreads = 32 * (kWarpX + kXWarps);
     static constexpr int kNAcc = 512 / (8 * kN);             // accumulator buffers (4 or 2)
     static constexpr uint32_t kTmemCols = kNAcc * 8 * kN;    // all 512 columns
-    static constexpr int kCPJ = 2 * kMH;                     // TMEM columns per sub-block and pass
+    static constexpr int kCPJ = kCPM * kMH;                  // TMEM columns per sub-block and pass
     static constexpr int kJB = kCPJ <= 4 ? 8 : (kCPJ <= 8 ? 4 : (MT >= 16 ? 1 : 2));  // sub-blocks per TMEM wait
     static constexpr int kBStepBytes = kN * 128;
     static constexpr int kOffA = 0;                                            // 1024-aligned
@@ -126,10 +130,10 @@ __device__ __forceinline__ uint32_t sw128_offset(int n, int chunk) {
 }
 
 template <int MT, bool XB>
-__global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<MT, XB>::kThreads, 1)
     q4k_tcgemv_kernel(const __grid_constant__ WeightGroup grp, const void* __restrict__ X, int M, int K,
                       int C, int kb_per, int pdl_flags, unsigned long long* amax, unsigned int* err) {
-    using Cfg = TcCfg<MT>;
+    using Cfg = TcCfg<MT, XB>;
     constexpr int WS = Cfg::kWS, AS = Cfg::kAS, BS = Cfg::kBS, HR = Cfg::kHR, N = Cfg::kN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                 const float* xsum = reinterpret_cast<const float*>(smem + Cfg::kOffXs) + hs * MT * 8;
                 const float* gf = reinterpret_cast<const float*>(smem + Cfg::kOffG) + hs * MT * 2;
                 const float d = half_lo(hd.x), dmin = half_hi(hd.x);
-                constexpr int MH = Cfg::kMH;
+                constexpr int MH = Cfg::kMH, CPM = Cfg::kCPM;
 #pragma unroll
                 for (int p0 = 0; p0 < MT; p0 += MH) {
                     float qa[MH], ma[MH];
@@ -357,15 +361,15 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
 #pragma unroll
                     for (int j0 = 0; j0 < 8; j0 += JB) {
                     // JB sub-blocks' loads in flight together, one wait
-                    uint32_t vb[JB][2 * MH];
+                    uint32_t vb[JB][CPM * MH];
 #pragma unroll
                     for (int jj = 0; jj < JB; ++jj)
-                        tmem_ld_32x32b(tl + static_cast<uint32_t>((u * 8 + j0 + jj) * N + 2 * p0), vb[jj]);
+                        tmem_ld_32x32b(tl + static_cast<uint32_t>((u * 8 + j0 + jj) * N + CPM * p0), vb[jj]);
                     tmem_ld_wait();
 #pragma unroll
                     for (int jj = 0; jj < JB; ++jj) {
                         const int j = j0 + jj;
-                        const uint32_t (&v)[2 * MH] = vb[jj];
+                        const uint32_t (&v)[CPM * MH] = vb[jj];
                         const uint32_t scw = j < 4 ? scb.sc_lo : scb.sc_hi;
                         const uint32_t mw = j < 4 ? scb.m_lo : scb.m_hi;
                         const float mj = byte_to_float(mw, j & 3);
@@ -373,7 +377,8 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                         const float scj = byte_to_float(scw, j & 3) * ((j & 1) ? 0.0625f : 1.f);
 #pragma unroll
                         for (int m = 0; m < MH; ++m) {
-                            const float sj = __uint_as_float(v[2 * m]) + __uint_as_float(v[2 * m + 1]);
+                            const float sj = CPM == 2 ? __uint_as_float(v[2 * m]) + __uint_as_float(v[CPM * m + 1])
+                                                      : __uint_as_float(v[m]);
                             qa[m] = fmaf(scj, sj, qa[m]);
                             ma[m] = fmaf(mj, xsum[(p0 + m) * 8 + j], ma[m]);
                         }
@@ -440,40 +445,49 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
         constexpr int XR = Cfg::kXRows;
         const int mx0 = (warp - Cfg::kWarpX) * XR;  // first activation row of this warp
         const int c = lane >> 3;
-        float nxt[XR][8];
-        auto load = [&](int sb, float (&v)[XR][8]) {
+        // a row's 8 activations as loaded: one uint4 (8 bf16) or two (8 fp32),
+        // kept packed while the next super-block's loads are in flight
+        constexpr int RW = XB ? 1 : 2;
+        uint4 nxt[XR][RW];
+        auto load = [&](int sb, uint4 (&v)[XR][RW]) {
             const int64_t k = static_cast<int64_t>(kb0 + sb % nb) * kBlockWeights + 8 * lane;
 #pragma unroll
             for (int m = 0; m < XR; ++m) {
                 const int mm = mx0 + m;
-                if (mm >= M) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[m][e] = 0.f;
-                } else if constexpr (XB) {
-                    const uint4 rw = __ldg(reinterpret_cast<const uint4*>(
-                        static_cast<const uint16_t*>(X) + static_cast<int64_t>(mm) * K + k));
-                    const uint32_t wv[4] = {rw.x, rw.y, rw.z, rw.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        v[m][2 * e] = __uint_as_float(wv[e] << 16);
-                        v[m][2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
-                    }
-                } else {
-                    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(X) +
-                                                                      static_cast<int64_t>(mm) * K + k);
-                    const float4 a = __ldg(p), b = __ldg(p + 1);
-                    v[m][0] = a.x; v[m][1] = a.y; v[m][2] = a.z; v[m][3] = a.w;
-                    v[m][4] = b.x; v[m][5] = b.y; v[m][6] = b.z; v[m][7] = b.w;
+                for (int h = 0; h < RW; ++h) {
+                    if (mm >= M)
+                        v[m][h] = make_uint4(0u, 0u, 0u, 0u);
+                    else if constexpr (XB)
+                        v[m][h] = __ldg(reinterpret_cast<const uint4*>(
+                            static_cast<const uint16_t*>(X) + static_cast<int64_t>(mm) * K + k));
+                    else
+                        v[m][h] = __ldg(reinterpret_cast<const uint4*>(
+                            static_cast<const float*>(X) + static_cast<int64_t>(mm) * K + k) + h);
                 }
+            }
+        };
+        auto unpack = [&](const uint4 (&w)[RW], float (&f)[8]) {
+            if constexpr (XB) {
+                const uint32_t wv[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    f[2 * e] = __uint_as_float(wv[e] << 16);
+                    f[2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
+                }
+            } else {
+                const uint32_t wv[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[RW - 1].x, w[RW - 1].y, w[RW - 1].z, w[RW - 1].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(wv[e]);
             }
         };
         if (total > 0) load(0, nxt);
         for (int sb = 0; sb < total; ++sb) {
-            float cur[XR][8];
+            uint4 curw[XR][RW];
 #pragma unroll
             for (int m = 0; m < XR; ++m)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) cur[m][e] = nxt[m][e];
+                for (int h = 0; h < RW; ++h) curw[m][h] = nxt[m][h];
             if (sb + 1 < total) load(sb + 1, nxt);
             const int hs = sb % HR;
             // the slots of this super-block's four chunks and its side-data entry
@@ -490,12 +504,14 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
 #pragma unroll
             for (int m = 0; m < XR; ++m) {
                 const int mm = mx0 + m;
+                float cur[8];
+                unpack(curw[m], cur);
                 uint32_t amax_bits = 0;
                 float sum = 0.f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    amax_bits = max(amax_bits, __float_as_uint(cur[m][e]) & 0x7FFFFFFFu);
-                    sum += cur[m][e];
+                    amax_bits = max(amax_bits, __float_as_uint(cur[e]) & 0x7FFFFFFFu);
+                    sum += cur[e];
                 }
                 amax_bits = __reduce_max_sync(0xffffffffu, amax_bits);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 1);
@@ -512,15 +528,16 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
                 for (int p = 0; p < 4; ++p) {
                     // positions 2p, 2p+1 of this lane's 8 take k (0, 2), (1, 3), (4, 6), (5, 7)
                     const int ka = (p & 1) + 4 * (p >> 1), kb = ka + 2;
-                    const float xa = (cur[m][ka] * s1) * s2, xb = (cur[m][kb] * s1) * s2;
+                    const float xa = (cur[ka] * s1) * s2, xb = (cur[kb] * s1) * s2;
                     const __nv_bfloat162 hh = __floats2bfloat162_rn(xa, xb);
                     const float2 hf = __bfloat1622float2(hh);
                     const __nv_bfloat162 ll = __floats2bfloat162_rn(xa - hf.x, xb - hf.y);
                     hw[p] = *reinterpret_cast<const uint32_t*>(&hh);
                     lw[p] = *reinterpret_cast<const uint32_t*>(&ll);
                 }
-                *reinterpret_cast<uint4*>(bt + sw128_offset(2 * mm, lane & 7)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(bt + sw128_offset(2 * mm + 1, lane & 7)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                *reinterpret_cast<uint4*>(bt + sw128_offset(Cfg::kCPM * mm, lane & 7)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                if constexpr (Cfg::kLo)
+                    *reinterpret_cast<uint4*>(bt + sw128_offset(2 * mm + 1, lane & 7)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 if ((lane & 3) == 0) xsum[mm * 8 + (lane >> 2)] = sum;
                 if (lane == 0) {
                     gf[2 * mm] = g1;
@@ -547,7 +564,7 @@ __global__ void __launch_bounds__(TcCfg<MT>::kThreads, 1)
 
 template <int MT, bool XB>
 static cudaError_t tc_set_attr(DeviceInfo& dev, int slot) {
-    using Cfg = TcCfg<MT>;
+    using Cfg = TcCfg<MT, XB>;
     cudaError_t e = cudaFuncSetAttribute(q4k_tcgemv_kernel<MT, XB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
@@ -590,7 +607,7 @@ cudaError_t tcgemv_setup(DeviceInfo& dev) {
 template <int MT, bool XB>
 static cudaError_t tc_launch_mt(const WeightGroup& grp, const void* X, int M, int K, cudaStream_t stream,
                                 const DeviceInfo& dev, int slot, int pdl, unsigned long long* amax) {
-    using Cfg = TcCfg<MT>;
+    using Cfg = TcCfg<MT, XB>;
     const int KB = K / kBlockWeights;
     const int tiles = grp.tile_start[grp.count];
     const int slots = dev.num_sms * dev.tc_occ[XB ? 1 : 0][slot];
@@ -642,7 +659,7 @@ static cudaError_t tc_launch_mt(const WeightGroup& grp, const void* X, int M, in
 
 cudaError_t launch_tcgemv(const WeightGroup& grp, const void* X, bool x_bf16, int M, int K,
                           cudaStream_t stream, const DeviceInfo& dev, int pdl, unsigned long long* amax) {
-    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
+    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 0;
 #define Q4K_CASE(MT, SLOT)                                                                  \
     case MT:                                                                                \
         return x_bf16 ? tc_launch_mt<MT, true>(grp, X, M, K, stream, dev, SLOT, pdl, amax)  \

@@ -87,10 +87,12 @@ int q4k_dequant(const void* W, int64_t N, int64_t K, float* out_f32, void* strea
  * each linear layer of a K-quant model emits ("rlx-qwen3" crate page, the
  * packed-GGUF note under "Quick start"; "rlx-llama32" crate page, section
  * "Packed GGUF"), with the weights dequantised inside the kernel.
- * M <= 16 (decode) runs the split-K GEMV kernel; larger M runs it over
- * 16-row slices of X, which reads W once per slice (fp32 prefill costs
- * ceil(M/16) weight sweeps; bf16 activations through q4k_matmul_bf16 read W
- * once). Accuracy: |Y - exact| <= 1e-4 * sum_k |X*w| per output.
+ * M <= 16 (decode) runs one decode launch (M <= 2: the CUDA-core GEMV; 3..16:
+ * the tensor-core kernel, fp32 accuracy kept by splitting X into bf16 hi +
+ * lo); larger M runs it over 16-row slices of X, which reads W once per slice
+ * (fp32 prefill costs ceil(M/16) weight sweeps; bf16 activations through
+ * q4k_matmul_bf16 read W once). Accuracy: |Y - exact| <= 1e-4 * sum_k |X*w|
+ * per output.
  *   W  device, N*K/256*144 bytes; X device, M*K floats; Y device, M*N floats;
  *   all 16-byte aligned.
  */
@@ -101,7 +103,8 @@ int q4k_matmul(const void* W, int64_t N, int64_t K, const float* X, int64_t M, f
  * Y = X * W^T with bfloat16 activations X_bf16 [M][K] (bit patterns): the same
  * packed-weight matmul ("rlx-llama32" crate page, section "Packed GGUF") for a
  * block of token rows, as the chunked prefill of the nx_f32_llm_run_v3 listing
- * issues it. M <= 16 runs the split-K GEMV kernel (accuracy 1e-4 *
+ * issues it. M <= 16 runs the decode kernels (M <= 2 on the CUDA cores, 3..16
+ * on the tensor cores with the 4-bit codes as the MMA operand; accuracy 1e-4 *
  * sum|X*w|); M >= 17 (chunked prefill) runs the tcgen05 tensor-core GEMM,
  * which rounds the dequantised weights to bfloat16 (accuracy 5e-3 * sum|X*w|).
  *   W  device, N*K/256*144 bytes; X_bf16 device, M*K uint16; Y device, M*N

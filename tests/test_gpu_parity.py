@@ -214,11 +214,14 @@ def test_gemm_rows_beyond_one_launch(q4k, oracle_mod):
     assert worst <= 1.0, f"max |err| / ({TOL_GEMM} * sum|wx|) = {worst:.3f}"
 
 
-def test_dispatch_boundary_16_17(q4k, oracle_mod):
+def test_dispatch_boundaries(q4k, oracle_mod):
+    """Rows 1..2: CUDA-core GEMV; 3..16: the tensor-core decode kernel, both
+    held to the GEMV bar; 17 up: the GEMM."""
     N, K = 160, 512
     Wh = synth.weight_rows(7000, N, K)
     Wd = Wh.to(DEV)
-    for M, tol in ((16, TOL_GEMV), (17, TOL_GEMM)):
+    for M, tol in ((2, TOL_GEMV), (3, TOL_GEMV), (16, TOL_GEMV), (17, TOL_GEMM), (32, TOL_GEMM),
+                   (33, TOL_GEMM)):
         X = synth.activations(7001 + M, M, K, torch.bfloat16)
         _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X, tol)
 
