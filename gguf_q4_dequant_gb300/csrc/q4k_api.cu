@@ -205,12 +205,15 @@ int encode_w(CUtensorMap* map, const void* W, int64_t N, int64_t K, int rows) {
 }
 
 // X as a 2-D bf16 tensor {K, M}; box {64, BN} with the 128-byte swizzle.
+// X [M][K] bf16 as a 3-D tensor {64 k, M rows, K / 64 blocks of 64 k} (strides
+// 2K bytes per row, 128 bytes per k block): a box {64, BN, s} lands as s
+// consecutive k-major, 128-byte-swizzled tiles of BN rows x 64 k.
 int encode_x_bf16_uncached(CUtensorMap* map, const void* X, int64_t M, int64_t K, int BN) {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BN)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims,
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BN), static_cast<cuuint32_t>(gemm_x_steps(BN))};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(X), dims,
                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -11,19 +11,33 @@
 //   accumulator    = 128 TMEM lanes x BN fp32 columns
 // so each dequantised weight tile is reused across all BN tokens of the tile.
 //
-// Warp roles (576 threads, one CTA per SM):
-//   warp 0      TMA producer: packed W super-block tiles {144 B, 128 rows}
-//               (their own ring) and X tiles {64 k, BN rows} (128-byte
-//               swizzle, into the k-step ring); both rings refilled as soon as
-//               a slot frees
-//   warp 1      TMEM allocator and MMA issuer (the warp runs the loop, one
-//               elected lane issues: 4 MMAs of K = 16 and one commit per step)
-//   warps 2..17 dequantisers (thread t <-> weight row t % 128; t / 128 picks
-//               the nibble half and which 16 of the chunk's 32 qs bytes): read
-//               a super-block's bytes into registers and write 16 bf16 weights
-//               per k-step into the swizzled A tile; then the epilogue (TMEM ->
-//               registers -> Y, 128-byte coalesced stores per token column;
-//               four warps per TMEM lane quadrant).
+// Warp roles (640 threads, one CTA per SM):
+//   warp 0      TMA producer of the packed W super-block tiles {144 B, 128
+//               rows}, into their own ring, refilled as the dequantisers
+//               release a stage
+//   warp 19     TMA producer of the X tiles (k-major, 128-byte swizzle, into
+//               the k-step ring): one copy brings kXSteps consecutive 64-k
+//               tiles of BN token rows ({64 k, BN rows, kXSteps} of a 3-D view
+//               of X), refilled as the MMAs release the stages. (A TMA issue
+//               costs its thread 150-350 cycles; one copy per 64-k step, from
+//               a thread that also fed the W ring, came only every ~800
+//               cycles, slower than the MMAs of a small-BN step.)
+//   warps 1, 18 MMA issuers: warp 1 takes the even k-steps, warp 18 the odd
+//               ones, each into its own TMEM accumulator (the epilogue adds
+//               the two), so the barrier waits and issue latencies of two
+//               steps overlap (the warp runs the loop, one elected lane
+//               issues: 4 MMAs of K = 16 and one commit per step); warp 1
+//               also allocates TMEM
+//   warps 2..17 dequantisers, four groups of 128 threads: thread t <-> weight
+//               row t % 128 of the 64-k chunk c = t / 128 of every super-block
+//               (k-step 4 sb + c). A thread reads its row's header and the
+//               chunk's 32 qs bytes into registers, releases the W stage, and
+//               writes the whole 128-byte A row of its k-step (64 bf16
+//               weights, both nibble halves): one stage wait, one proxy fence
+//               and one arrival per 64 weights. The four chunks of a
+//               super-block are dequantised in parallel. Then the epilogue
+//               (TMEM -> registers -> Y, 128-byte coalesced stores per token
+//               column; four warps per TMEM lane quadrant).
 // When the tiles alone cannot fill the GPU, K is split across a thread-block
 // cluster of C CTAs: each CTA pushes the accumulator rows owned by rank r
 // (rows [r*rows, (r+1)*rows), rows = ceil(128/C) rounded up to a multiple of 4)
@@ -40,29 +54,58 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmKStep = 64;                       // bf16 k per A/B stage (one 128-byte row)
 constexpr int kGemmDequantWarps = 16;
 constexpr int kGemmDequantThreads = 32 * kGemmDequantWarps;   // 512
-constexpr int kGemmThreads = 64 + kGemmDequantThreads;        // 576
-constexpr int kGemmWStages = 3;  // a DRAM round trip is longer than one super-block of MMAs
+constexpr int kGemmWarpMma2 = 2 + kGemmDequantWarps;          // the second MMA warp (18)
+constexpr int kGemmWarpX = kGemmWarpMma2 + 1;                  // the X producer (19)
+constexpr int kGemmThreads = 32 * (kGemmWarpX + 1);            // 640
 constexpr int kGemmWStageBytes = kGemmBM * kBlockBytes;   // 18432
 constexpr int kGemmAStageBytes = kGemmBM * 128;           // 16384
 
 // One ring of k-steps, each holding a dequantised A tile and a TMA-loaded X
 // (B) tile, as deep as shared memory allows: a step's full barrier completes
-// when its X bytes have landed and every dequantising thread has arrived, and
-// one MMA commit releases both tiles, so the MMA-issuing warp waits once and
-// commits once per step.
+// when its X bytes have landed and its dequantising group has arrived, and
+// one MMA commit releases both tiles, so an MMA-issuing warp waits once and
+// commits once per step. Each MMA warp has its own full barrier per stage
+// (k-step ks: warp ks % 2), visited every lcm(2, S) steps.
+//
+// Release barriers: an mbarrier wait names only the parity of the phase it
+// waits for, so a waiter must never find its barrier two phases behind that
+// phase. A dequantising group writes every fourth k-step; with a ring of S < 4
+// stages a per-stage release barrier could be two phases behind when the group
+// comes back to the stage. So the release of k-step ks (the commit of k-step
+// ks - S) goes to a barrier of its own pair (group ks % 4, stage ks % S): the
+// group visits that pair every L = lcm(4, S) steps and each visit is released
+// by exactly one commit, the (ks - S) / L -th on that barrier. The producer
+// waits on the same barriers for the X tiles. Both barrier families see one
+// MMA warp each (L is even), so their phases follow the steps in order.
 template <int BN>
 struct GemmCfg {
-    static constexpr int kStages = BN == 256 ? 3 : BN == 128 ? 5 : BN == 64 ? 6 : 8;
+    static constexpr int kStages = BN == 256 ? 3 : 4;
+    // 64-k steps per X copy (the stages of one copy are consecutive in the ring)
+    static constexpr int kXSteps = BN == 256 ? 1 : 4;
+    static_assert(kStages % kXSteps == 0, "X copies tile the ring");
+    static constexpr int kXSlots = kStages / kXSteps;  // X copies in flight
+    // X-full barriers: with kXSteps > 1 (even) both MMA warps wait on every
+    // copy, one barrier per slot; with one step per copy each warp waits only
+    // on its own steps' copies, so (as for the A tiles) one per (warp, stage)
+    static constexpr int kXBars = kXSteps == 1 ? 2 * kStages : kXSlots;
+    // packed-W ring (super-blocks), the rest of shared memory: a W box takes
+    // ~3.5 us from issue to landing under load (measured), so the ring, not
+    // the MMAs or the dequantisers, sets the pace of a narrow tile
+    static constexpr int kWStages = BN == 256 ? 4 : BN == 128 ? 5 : BN == 64 ? 7 : 8;
+    static constexpr int kL = kStages % 4 == 0 ? kStages : kStages % 2 == 0 ? 2 * kStages : 4 * kStages;  // lcm(4, S)
+    static constexpr int kL2 = kStages % 2 == 0 ? kStages : 2 * kStages;  // lcm(2, S)
     static constexpr int kBStageBytes = BN * 128;
     static constexpr int kOffA = 0;                                            // 1024-aligned
     static constexpr int kOffB = kOffA + kStages * kGemmAStageBytes;           // 1024-aligned
     static constexpr int kOffW = kOffB + kStages * kBStageBytes;
-    static constexpr int kOffBar = kOffW + kGemmWStages * kGemmWStageBytes;
-    // barriers: w_full[W], w_empty[W], full[S], empty[S], acc_full
-    static constexpr int kNumBars = 2 * kGemmWStages + 2 * kStages + 1;
+    static constexpr int kOffBar = kOffW + kWStages * kGemmWStageBytes;
+    // barriers: w_full[W], w_empty[W], full[2][S] (A tiles), release[4][S],
+    // x_full[kXBars], acc_full
+    static constexpr int kNumBars = 2 * kWStages + 6 * kStages + kXBars + 1;
     static constexpr int kOffTmem = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffTmem + 16 + 1024;   // + alignment slack
-    static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+    static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of BN columns
     // split-K slots: C <= 8 slots of BN x rows floats in the A/B region, rows =
     // ceil(128 / C) rounded up to a multiple of 4; C * rows <= 144 for C <= 8
     static_assert((kGemmBM + 16) * BN * 4 <= kOffW, "split-K slots must fit in the A/B region");
@@ -96,12 +139,27 @@ __device__ __forceinline__ uint4 dequant8x(uint64_t P, int hh, uint64_t d1s0, ui
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// 32 columns of a lane's accumulator row: the sum of the two MMA warps'
+// accumulators (columns c and BN + c), 16 columns of each per load.
+template <int BN>
+__device__ __forceinline__ void load_acc_sum(uint32_t taddr, float (&v)[32]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t a[16], b[16];
+        tmem_ld_32x32b(taddr + 16 * h, a);
+        tmem_ld_32x32b(taddr + BN + 16 * h, b);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[16 * h + j] = __uint_as_float(a[j]) + __uint_as_float(b[j]);
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     q4k_gemm_kernel(const __grid_constant__ WeightGroup grp, const __grid_constant__ CUtensorMap tmapX,
                 int M, int K, int C, int kb_per, int pdl_flags, unsigned int* err) {
     using Cfg = GemmCfg<BN>;
-    constexpr int S = Cfg::kStages;
+    constexpr int S = Cfg::kStages, WS = Cfg::kWStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -123,22 +181,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int ks0 = 4 * kb0;
 
     const uint32_t bw_full = sbase + Cfg::kOffBar;
-    const uint32_t bw_empty = bw_full + 8 * kGemmWStages;
-    const uint32_t bfull = bw_empty + 8 * kGemmWStages;
-    const uint32_t bempty = bfull + 8 * S;
-    const uint32_t bacc = bempty + 8 * S;
+    const uint32_t bw_empty = bw_full + 8 * WS;
+    const uint32_t bfull = bw_empty + 8 * WS;
+    const uint32_t brel = bfull + 8 * 2 * S;  // [4][S], see GemmCfg
+    const uint32_t bxfull = brel + 8 * 4 * S;  // [kXBars], see GemmCfg
+    const uint32_t bacc = bxfull + 8 * Cfg::kXBars;
+    constexpr int XS = Cfg::kXSteps, XQ = Cfg::kXSlots;
+    // the full barrier of X copy j and the parity of its phase
+    auto xfull_bar = [&](int j) {
+        return bxfull + 8u * static_cast<uint32_t>(XS == 1 ? (j & 1) * S + j % S : j % XQ);
+    };
+    auto xfull_parity = [](int j) { return static_cast<uint32_t>((XS == 1 ? j / Cfg::kL2 : j / XQ) & 1); };
+    // the release barrier of k-step ks, and the parity of its phase (ks >= S)
+    auto rel_bar = [&](int ks) { return brel + 8u * static_cast<uint32_t>((ks & 3) * S + ks % S); };
+    auto rel_parity = [](int ks) { return static_cast<uint32_t>(((ks - S) / Cfg::kL) & 1); };
+    // the full barrier of k-step ks's A tile (MMA warp ks % 2) and the parity of its phase
+    auto full_bar = [&](int ks) { return bfull + 8u * static_cast<uint32_t>((ks & 1) * S + ks % S); };
+    auto full_parity = [](int ks) { return static_cast<uint32_t>((ks / Cfg::kL2) & 1); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmem);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kGemmWStages; ++i) {
+        for (int i = 0; i < WS; ++i) {
             mbar_init(bw_full + 8 * i, 1);
             mbar_init(bw_empty + 8 * i, kGemmDequantThreads);
         }
-        for (int i = 0; i < S; ++i) {
-            mbar_init(bfull + 8 * i, kGemmDequantThreads + 1);  // + the producer's expect_tx arrival
-            mbar_init(bempty + 8 * i, 1);
-        }
-        mbar_init(bacc, 1);
+        for (int i = 0; i < 2 * S; ++i) mbar_init(bfull + 8 * i, kGemmBM);  // one dequantising group
+        for (int i = 0; i < Cfg::kXBars; ++i) mbar_init(bxfull + 8 * i, 1);  // the X producer, with the bytes
+        for (int i = 0; i < 4 * S; ++i) mbar_init(brel + 8 * i, 1);  // one MMA commit
+        mbar_init(bacc, 2);  // the last commit of each MMA warp
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -153,85 +223,73 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // epilogue assignment of the dequantising warps (set in their branch)
     bool acc_ok = false;
     int epi_cols = 0, epi_c0 = 0, epi_row = 0;
-    // Every warp except the producer waits for the preceding grid here; the
-    // producer waits before its first activation load (and, unless weight
-    // prefetch is allowed, before its first weight load).
+    // Every warp except the W producer waits for the preceding grid here; the
+    // W producer waits only unless weight prefetch is allowed.
     if (warp != 0) pdl_wait();
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer ---
+        // ---------------------------------------------- W producer (TMA) ---
         if (lane == 0) {
             tma_prefetch_desc(tmapW);
-            tma_prefetch_desc(&tmapX);
             const uint64_t pol_w = policy_evict_first();
-            const uint64_t pol_x = policy_evict_last();
             if (pdl_flags & 1) pdl_wait();
-            // The W ring (refilled when the dequantisers release a stage) and
-            // the X ring (refilled when the MMA of a stage completes) advance
-            // independently: the thread polls both and never blocks on one
-            // while the other could be refilled. Bounded like mbar_wait.
-            bool x_ready = (pdl_flags & 1) != 0;  // preceding grid already complete
-            int sb = 0, ks = 0;
-            uint32_t idle = 0;
-            unsigned long long t0 = 0;
-            while (sb < KB || ks < nks) {
-                bool progress = false;
-                if (sb < KB) {
-                    const int ws = sb % kGemmWStages;
-                    if (mbar_test_wait(bw_empty + 8 * ws, ((sb / kGemmWStages) & 1) ^ 1)) {
-                        mbar_arrive_expect_tx(bw_full + 8 * ws, kGemmWStageBytes);
-                        tma_load_2d_hint(sbase + Cfg::kOffW + ws * kGemmWStageBytes, tmapW,
-                                         (kb0 + sb) * kBlockBytes, n0, bw_full + 8 * ws, pol_w);
-                        ++sb;
-                        progress = true;
-                    }
-                }
-                if (ks < nks) {
-                    const int s = ks % S;
-                    if (mbar_test_wait(bempty + 8 * s, ((ks / S) & 1) ^ 1)) {
-                        if (!x_ready) {
-                            pdl_wait();
-                            x_ready = true;
-                        }
-                        mbar_arrive_expect_tx(bfull + 8 * s, Cfg::kBStageBytes);
-                        tma_load_2d_hint(sbase + Cfg::kOffB + s * Cfg::kBStageBytes, &tmapX,
-                                         (ks0 + ks) * kGemmKStep, m0, bfull + 8 * s, pol_x);
-                        ++ks;
-                        progress = true;
-                    }
-                }
-                if (progress) {
-                    idle = 0;
-                } else if (idle++ == 0) {
-                    t0 = globaltimer();
-                } else if ((idle & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
-                    atomicOr(err, 1u);
-                    break;
-                }
+            int sb = 0;
+            for (; sb < KB; ++sb) {
+                const int ws = sb % WS;
+                if (!mbar_wait(bw_empty + 8 * ws, ((sb / WS) & 1) ^ 1, err)) break;
+                mbar_arrive_expect_tx(bw_full + 8 * ws, kGemmWStageBytes);
+                tma_load_2d_hint(sbase + Cfg::kOffW + ws * kGemmWStageBytes, tmapW,
+                                 (kb0 + sb) * kBlockBytes, n0, bw_full + 8 * ws, pol_w);
             }
             // On a timeout the CTA must still not exit while a copy it issued is
-            // landing. A W stage (X step) is issued only after its previous use
-            // was released, which follows the landing of that use's bytes, so
-            // at most the last kGemmWStages W stages and S X steps issued can be
-            // in flight: wait for exactly those (the X steps' barriers also count
-            // the dequantisers' arrivals, hence the short limit: by then the
-            // copy has landed even if the dequantisers gave up).
-            if (sb < KB || ks < nks) {
-                for (int i = sb - kGemmWStages < 0 ? 0 : sb - kGemmWStages; i < sb; ++i)
-                    mbar_wait(bw_full + 8 * (i % kGemmWStages), (i / kGemmWStages) & 1, err, kDrainLimitNs);
-                for (int i = ks - S < 0 ? 0 : ks - S; i < ks; ++i)
-                    mbar_wait(bfull + 8 * (i % S), (i / S) & 1, err, kDrainLimitNs);
-            }
+            // landing. A stage is reissued only after its previous use was
+            // released, which follows the landing of that use's bytes, so at
+            // most the last WS stages issued can be in flight: wait for those.
+            if (sb < KB)
+                for (int i = sb - WS < 0 ? 0 : sb - WS; i < sb; ++i)
+                    mbar_wait(bw_full + 8 * (i % WS), (i / WS) & 1, err, kDrainLimitNs);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------- MMA issuer ---
+    } else if (warp == kGemmWarpX) {
+        // ---------------------------------------------- X producer (TMA) ---
+        // (after the preceding grid, like every warp but 0: X is its output).
+        // Copy j fills the stages of k-steps XS*j .. XS*j + XS - 1; they are
+        // free once the MMAs of the steps S earlier completed: the last even
+        // and the last odd of them (each MMA warp completes its steps in order).
+        if (lane == 0) {
+            tma_prefetch_desc(&tmapX);
+            const uint64_t pol_x = policy_evict_last();
+            const int nx = nks / XS;
+            int j = 0;
+            for (; j < nx; ++j) {
+                const int klast = XS * j + XS - 1;
+                bool ok = true;
+                for (int k = klast - (XS > 1 ? 1 : 0); k <= klast && ok; ++k)
+                    ok = k < S || mbar_wait(rel_bar(k), rel_parity(k), err);
+                if (!ok) break;
+                const uint32_t xb = xfull_bar(j);
+                mbar_arrive_expect_tx(xb, XS * Cfg::kBStageBytes);
+                tma_load_3d_hint(sbase + Cfg::kOffB + ((XS * j) % S) * Cfg::kBStageBytes, &tmapX, 0, m0,
+                                 ks0 + XS * j, xb, pol_x);
+            }
+            // as for W: at most the last XQ copies issued can be landing
+            if (j < nx)
+                for (int i = j - XQ < 0 ? 0 : j - XQ; i < j; ++i)
+                    mbar_wait(xfull_bar(i), xfull_parity(i), err, kDrainLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == 1 || warp == kGemmWarpMma2) {
+        // ------------------------------------------------ MMA issuers ---
         // The whole warp runs the loop and the waits (so stage indices and
-        // descriptors stay warp-uniform); one elected lane issues.
+        // descriptors stay warp-uniform); one elected lane issues. Warp
+        // mw = 0 / 1 takes k-steps mw, mw + 2, ... into accumulator mw.
         constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, BN);
-        for (int ks = 0; ks < nks; ++ks) {
+        const int mw = warp == 1 ? 0 : 1;
+        const uint32_t dacc = tmem + static_cast<uint32_t>(mw * BN);
+        for (int ks = mw; ks < nks; ks += 2) {
             const int s = ks % S;
-            const bool ok = mbar_wait(bfull + 8 * s, (ks / S) & 1, err);
+            const bool ok = mbar_wait(xfull_bar(ks / XS), xfull_parity(ks / XS), err) &&
+                            mbar_wait(full_bar(ks), full_parity(ks), err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             if (elect_one()) {
@@ -239,8 +297,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint64_t b0 = sw128_desc(sbase + Cfg::kOffB + s * Cfg::kBStageBytes);
 #pragma unroll
                 for (int kk = 0; kk < kGemmKStep / 16; ++kk)  // +32 bytes per k16 = +2 in the address field
-                    tc_mma_bf16(tmem, a0 + 2 * kk, b0 + 2 * kk, idesc, (ks | kk) != 0);
-                tc_commit(bempty + 8 * s);
+                    tc_mma_bf16(dacc, a0 + 2 * kk, b0 + 2 * kk, idesc, (ks >= 2) || kk != 0);
+                tc_commit(rel_bar(ks + S));  // releases the stage for k-step ks + S
             }
             __syncwarp();
         }
@@ -250,46 +308,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------ dequantisers (A) ---
         const int t = threadIdx.x - 64;
         const int r = t & (kGemmBM - 1);  // weight row within the tile
-        const int hh = (t >> 7) & 1;      // 0: low nibbles (sub-block 2c), 1: high (2c+1)
-        const int p = t >> 8;             // which 16 of the chunk's 32 qs bytes
+        const int c = t >> 7;             // 64-k chunk of the super-block (warp-uniform)
         bool ok = true;
         for (int sb = 0; sb < KB && ok; ++sb) {
-            const int ws = sb % kGemmWStages;
-            if (!mbar_wait(bw_full + 8 * ws, (sb / kGemmWStages) & 1, err)) { ok = false; break; }
-            // everything this thread needs from the packed super-block (its
-            // 4 x 16 qs bytes and the 8 scale factors) is read into registers
-            // at once and the W stage released, so the per-step chain below
-            // holds no shared-memory load
+            const int ws = sb % WS;
+            if (!mbar_wait(bw_full + 8 * ws, (sb / WS) & 1, err)) { ok = false; break; }
+            // the row's header and the chunk's 32 qs bytes into registers at
+            // once, and the W stage released before any arithmetic. The proxy
+            // fence orders these generic-proxy reads before the TMA (async
+            // proxy) write that reuses the stage: without it the release could
+            // land, and the next super-block overwrite the stage, before the
+            // reads had returned (seen as sporadic stale rows with 3-stage rings)
             const uint8_t* P = smem + Cfg::kOffW + ws * kGemmWStageBytes + r * kBlockBytes;
             const uint4 hd = *reinterpret_cast<const uint4*>(P);
-            ulonglong2 qv[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) qv[c] = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c + 16 * p);
+            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(P + 16 + 32 * c);
+            const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(P + 32 + 32 * c);
+            fence_proxy_async_smem();
             mbar_arrive(bw_empty + 8 * ws);
             const ScaleBytes scb = decode_scales(hd.y, hd.z, hd.w);
             const float d = half_lo(hd.x), dmin = half_hi(hd.x);
+            const uint64_t qw[4] = {qa.x, qa.y, qb.x, qb.y};  // qs bytes 8v .. 8v+7 of the chunk
+            uint4 o[2][4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int ks = sb * 4 + c;
-                const int s = ks % S;
-                const int j = 2 * c + hh;  // sub-block
+            for (int hh = 0; hh < 2; ++hh) {
+                // low nibbles (hh = 0) are sub-block 2c, k = b; high nibbles sub-block
+                // 2c + 1, k = 32 + b, for qs byte b of the chunk
+                const int j = 2 * c + hh;
                 const uint32_t scw = j < 4 ? scb.sc_lo : scb.sc_hi;
                 const uint32_t mw = j < 4 ? scb.m_lo : scb.m_hi;
                 const float d1 = d * byte_to_float(scw, j & 3);
                 const float m1 = dmin * byte_to_float(mw, j & 3);
                 const float d1s0 = d1 * exp2i(-4 * hh), d1s1 = d1 * exp2i(-8 - 4 * hh);
                 const uint64_t D0 = pack2(d1s0, d1s0), D1 = pack2(d1s1, d1s1), NM = pack2(-m1, -m1);
-                const uint4 o0 = dequant8x(qv[c].x, hh, D0, D1, NM);
-                const uint4 o1 = dequant8x(qv[c].y, hh, D0, D1, NM);
-                if (!mbar_wait(bempty + 8 * s, ((ks / S) & 1) ^ 1, err)) { ok = false; break; }
-                // output chunk 4hh + 2p + v holds k = 32hh + 16p + 8v .. +7 of this 64-k step
-                uint8_t* arow = smem + Cfg::kOffA + s * kGemmAStageBytes + r * 128;
-                const int sw = r & 7;
-                *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p) ^ sw) << 4)) = o0;
-                *reinterpret_cast<uint4*>(arow + (((4 * hh + 2 * p + 1) ^ sw) << 4)) = o1;
-                fence_proxy_async_smem();
-                mbar_arrive(bfull + 8 * s);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) o[hh][v] = dequant8x(qw[v], hh, D0, D1, NM);
             }
+            const int ks = sb * 4 + c;
+            const int s = ks % S;
+            if (ks >= S && !mbar_wait(rel_bar(ks), rel_parity(ks), err)) { ok = false; break; }
+            // 16-byte chunk 4hh + v of the A row holds k = 32hh + 8v .. +7
+            uint8_t* arow = smem + Cfg::kOffA + s * kGemmAStageBytes + r * 128;
+            const int sw = r & 7;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    *reinterpret_cast<uint4*>(arow + (((4 * hh + v) ^ sw) << 4)) = o[hh][v];
+            fence_proxy_async_smem();
+            mbar_arrive(full_bar(ks));
         }
 
         // ------------------------------------------------- epilogue ---
@@ -306,14 +372,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int n = n0 + epi_row;
 #pragma unroll 1
                 for (int cc = epi_c0; cc < epi_c0 + epi_cols; cc += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + cc, v);
-                    tmem_ld_wait();
+                    float v[32];
+                    load_acc_sum<BN>(tmem + (static_cast<uint32_t>(32 * q) << 16) + cc, v);
                     if (n < N) {
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) {
                             const int m = m0 + cc + jj;
-                            if (m < M) Y[static_cast<int64_t>(m) * N + n] = __uint_as_float(v[jj]);
+                            if (m < M) Y[static_cast<int64_t>(m) * N + n] = v[jj];
                         }
                     }
                 }
@@ -338,13 +403,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                  4u * static_cast<uint32_t>(epi_row - owner * rows);
 #pragma unroll 1
             for (int cc = epi_c0; cc < epi_c0 + epi_cols; cc += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(epi_row & ~31) << 16) + cc, v);
-                tmem_ld_wait();
+                float v[32];
+                load_acc_sum<BN>(tmem + (static_cast<uint32_t>(epi_row & ~31) << 16) + cc, v);
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj)
-                    st_shared_cluster_f32(dst + 4u * static_cast<uint32_t>((cc + jj) * rows),
-                                          __uint_as_float(v[jj]));
+                    st_shared_cluster_f32(dst + 4u * static_cast<uint32_t>((cc + jj) * rows), v[jj]);
             }
         }
         cluster_sync_all();
@@ -423,6 +486,16 @@ GemmPlan gemm_plan(int M, int ntiles, int K, const DeviceInfo& dev) {
         }
     }
     return best;
+}
+
+int gemm_x_steps(int BN) {
+    switch (BN) {
+        case 32: return GemmCfg<32>::kXSteps;
+        case 64: return GemmCfg<64>::kXSteps;
+        case 128: return GemmCfg<128>::kXSteps;
+        case 256: return GemmCfg<256>::kXSteps;
+    }
+    return 1;
 }
 
 template <int BN>

@@ -459,6 +459,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 const float* inv = inv_ring + (s * MT + m0) * 2;
 #pragma unroll
                 for (int m = 0; m < ML; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
+                fence_proxy_async_smem();  // generic reads of the W stage before its next TMA write
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             }

@@ -68,8 +68,8 @@ cudaError_t launch_argmax_finish(unsigned long long* keys, int M, cudaStream_t s
 cudaError_t gemv_setup(DeviceInfo& dev);
 
 // tcgen05 GEMM for M >= 17 rows of bf16 activations over a group of weight
-// matrices (grp.maps as for the GEMV); tmapX: 2-D bf16 map {K, M}, box
-// {64, BN}, 128-byte swizzle.
+// matrices (grp.maps as for the GEMV); tmapX: 3-D bf16 map {64, M, K / 64},
+// box {64, BN, gemm_x_steps(BN)}, 128-byte swizzle.
 struct GemmPlan {
     int BN;      // tokens per tile (MMA N)
     int C;       // K-split factor (cluster size along z)
@@ -77,6 +77,9 @@ struct GemmPlan {
 };
 // ntiles: total 128-row weight tiles of the group.
 GemmPlan gemm_plan(int M, int ntiles, int K, const DeviceInfo& dev);
+// 64-k steps of X that one TMA copy of the GEMM brings for tile width BN: the
+// X tensor map is a 3-D view {64 k, M rows, K / 64} with box {64, BN, this}.
+int gemm_x_steps(int BN);
 cudaError_t launch_gemm(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K,
                         const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev, int pdl);
 // Sets the kernels' attributes and fills dev.gemm_clusters.

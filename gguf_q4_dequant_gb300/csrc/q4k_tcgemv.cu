@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(TcCfg<MT, XB>::kThreads, 1)
                 q[rr][1] = *reinterpret_cast<const uint4*>(P + 32 + 32 * c);
                 hd[rr] = c == 0 ? *reinterpret_cast<const uint4*>(P) : make_uint4(0u, 0u, 0u, 0u);
             }
+            fence_proxy_async_smem();  // generic reads of the stage before its next TMA write
             mbar_arrive(b_wempty + 8 * ws);
             if (c == 0) {  // the rows' headers, for the readout
                 const int hs = sb % HR;
