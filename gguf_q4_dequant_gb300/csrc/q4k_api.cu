@@ -268,13 +268,15 @@ int run_gemv(int count, const void* const* W, const int64_t* N, int64_t K, const
 }
 
 // One GEMM launch over `count` matrices sharing K and X, per chunk of at most
-// 65535 * 32 rows of X (the grid's y limit at the narrowest tile).
+// 65535 * 32 rows of X, fewer when the grid (weight tiles x token tiles of at
+// least 32 rows) would pass 2^31 - 1 CTAs.
 int run_gemm(int count, const void* const* W, const int64_t* N, int64_t K, const uint16_t* X,
              int64_t M, float* const* Y, cudaStream_t stream, const DeviceInfo& dev) {
     WeightGroup grp;
     int rc = make_group(&grp, count, W, N, K);
     if (rc != Q4K_OK) return rc;
-    constexpr int64_t kChunk = 65535LL * 32;
+    const int64_t by_grid = 32 * (((int64_t(1) << 31) - 1) / grp.tile_start[count]);
+    const int64_t kChunk = by_grid < 65535LL * 32 ? by_grid : 65535LL * 32;
     for (int64_t m0 = 0; m0 < M; m0 += kChunk) {
         const int mc = static_cast<int>(M - m0 < kChunk ? M - m0 : kChunk);
         const GemmPlan plan = gemm_plan(mc, grp.tile_start[count], static_cast<int>(K), dev);

@@ -167,13 +167,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t sbase = raw + pad;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // global weight tile blockIdx.x -> (matrix, 128-row tile of it)
-    const int mi = group_matrix(grp, blockIdx.x);
+    // blockIdx.x = (global weight tile) x (token tiles) + token tile: the CTAs of
+    // one weight tile are adjacent in launch order, so they run together and
+    // the tile's packed bytes come from DRAM once (the others hit L2)
+    const int mtiles = (M + BN - 1) / BN;
+    const int wt = static_cast<int>(blockIdx.x) / mtiles;
+    const int mi = group_matrix(grp, wt);
     const CUtensorMap* tmapW = &grp.maps[mi];
     const int N = grp.N[mi];
     float* __restrict__ Y = grp.Y[mi];
-    const int n0 = (blockIdx.x - grp.tile_start[mi]) * kGemmBM;
-    const int m0 = blockIdx.y * BN;
+    const int n0 = (wt - grp.tile_start[mi]) * kGemmBM;
+    const int m0 = (static_cast<int>(blockIdx.x) - wt * mtiles) * BN;
     const int rank = blockIdx.z;  // cluster rank along z = K-slice
     const int kb0 = rank * kb_per;
     const int KB = min(K / kBlockWeights, kb0 + kb_per) - kb0;  // super-blocks of this K-slice
@@ -538,7 +542,7 @@ template <int BN>
 static cudaError_t launch_bn(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K,
                              const GemmPlan& plan, cudaStream_t stream, unsigned int* err, int pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grp.tile_start[grp.count], (M + BN - 1) / BN, plan.C);
+    cfg.gridDim = dim3(grp.tile_start[grp.count] * ((M + BN - 1) / BN), 1, plan.C);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = GemmCfg<BN>::kSmem;
     cfg.stream = stream;
