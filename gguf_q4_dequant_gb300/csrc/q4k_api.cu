@@ -283,9 +283,10 @@ int run_gemm(int count, const void* const* W, const int64_t* N, int64_t K, const
         CUtensorMap tx;
         if ((rc = encode_x_bf16(&tx, X + m0 * K, mc, K, plan.BN)) != Q4K_OK) return rc;
         for (int i = 0; i < count; ++i) grp.Y[i] = Y[i] + m0 * N[i];
-        if (launch_gemm(grp, tx, mc, static_cast<int>(K), plan, stream, dev,
-                        g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
-            return Q4K_ERR_CUDA;
+        for (int p = 0; p < plan.nlaunch; ++p)
+            if (launch_gemm(grp, tx, mc, static_cast<int>(K), plan.BN, plan.part[p], stream, dev,
+                            g_pdl.load(std::memory_order_relaxed)) != cudaSuccess)
+                return Q4K_ERR_CUDA;
     }
     return Q4K_OK;
 }

@@ -157,7 +157,7 @@ __device__ __forceinline__ void load_acc_sum(uint32_t taddr, float (&v)[32]) {
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     q4k_gemm_kernel(const __grid_constant__ WeightGroup grp, const __grid_constant__ CUtensorMap tmapX,
-                int M, int K, int C, int kb_per, int pdl_flags, unsigned int* err) {
+                int M, int K, int tile0, int C, int kb_per, int pdl_flags, unsigned int* err) {
     using Cfg = GemmCfg<BN>;
     constexpr int S = Cfg::kStages, WS = Cfg::kWStages;
     extern __shared__ uint8_t smem_raw[];
@@ -167,17 +167,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t sbase = raw + pad;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // blockIdx.x = (global weight tile) x (token tiles) + token tile: the CTAs of
+    // blockIdx.x = (weight tile - tile0) x (token tiles) + token tile: the CTAs of
     // one weight tile are adjacent in launch order, so they run together and
     // the tile's packed bytes come from DRAM once (the others hit L2)
     const int mtiles = (M + BN - 1) / BN;
-    const int wt = static_cast<int>(blockIdx.x) / mtiles;
+    const int wt = tile0 + static_cast<int>(blockIdx.x) / mtiles;
     const int mi = group_matrix(grp, wt);
     const CUtensorMap* tmapW = &grp.maps[mi];
     const int N = grp.N[mi];
     float* __restrict__ Y = grp.Y[mi];
     const int n0 = (wt - grp.tile_start[mi]) * kGemmBM;
-    const int m0 = (static_cast<int>(blockIdx.x) - wt * mtiles) * BN;
+    const int m0 = (static_cast<int>(blockIdx.x) - (wt - tile0) * mtiles) * BN;
     const int rank = blockIdx.z;  // cluster rank along z = K-slice
     const int kb0 = rank * kb_per;
     const int KB = min(K / kBlockWeights, kb0 + kb_per) - kb0;  // super-blocks of this K-slice
@@ -459,34 +459,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Tile width BN (tokens) and K-split C for M token rows over `ntiles` 128-row
 // weight tiles, from a cost model fitted to measurements of this kernel: a CTA
 // costs ~4 us of launch, pipeline fill and epilogue plus ~0.38 us per 64-k
-// step whatever BN is (the dequantising warps set the pace), and a K-split adds
+// step whatever BN is (the dequantising side sets the pace), and a K-split adds
 // the DSMEM reduction (~0.5 us + 0.018 us per token column, twice that above
 // four ranks). Waves come from the number of clusters the occupancy API says
-// can be resident at once.
+// can be resident at once. A launch whose unsplit CTAs would end in a partial
+// wave may instead run as two: the tiles of the full waves unsplit, then the
+// remaining tiles split in K, so that the last wave is short (the second launch
+// starts when the first completes; ~2 us between them).
+namespace {
+struct PlanCost {
+    double cost;
+    int C, kb_per;
+};
+PlanCost best_split(int bi, int bn, int M, int ntiles, int KB, const DeviceInfo& dev) {
+    const int cs[6] = {1, 2, 3, 4, 6, 8};
+    PlanCost best{1e300, 1, KB};
+    const int mtiles = (M + bn - 1) / bn;
+    for (int c : cs) {
+        if (c > KB) break;
+        const int kb_per = (KB + c - 1) / c;
+        const int ce = (KB + kb_per - 1) / kb_per;
+        const int resident = dev.gemm_clusters[bi][ce];
+        if (resident < 1) continue;
+        const long clusters = static_cast<long>(ntiles) * mtiles;
+        const long waves = (clusters + resident - 1) / resident;
+        double per = 4.0 + 0.38 * 4.0 * kb_per;
+        if (ce > 1) per += (0.5 + 0.018 * bn) * (ce <= 4 ? 1.0 : 2.0);
+        const double cost = static_cast<double>(waves) * per;
+        if (cost < best.cost * 0.999) best = PlanCost{cost, ce, kb_per};
+    }
+    return best;
+}
+}  // namespace
+
 GemmPlan gemm_plan(int M, int ntiles, int K, const DeviceInfo& dev) {
     const int KB = K / kBlockWeights;
-    const int cs[6] = {1, 2, 3, 4, 6, 8};
-    GemmPlan best{32, 1, KB};
+    GemmPlan best{32, 1, {{0, ntiles, 1, KB}, {0, 0, 1, KB}}};
     double best_cost = 1e300;
     for (int bi = 0; bi < 4; ++bi) {
         const int bn = 32 << bi;
         if (bn > 32 && bn / 2 >= M) break;  // a narrower tile already covers M
         const int mtiles = (M + bn - 1) / bn;
-        for (int c : cs) {
-            if (c > KB) break;
-            const int kb_per = (KB + c - 1) / c;
-            const int ce = (KB + kb_per - 1) / kb_per;
-            const int resident = dev.gemm_clusters[bi][ce];
-            if (resident < 1) continue;
-            const long clusters = static_cast<long>(ntiles) * mtiles;
-            const long waves = (clusters + resident - 1) / resident;
-            double per = 4.0 + 0.38 * 4.0 * kb_per;
-            if (ce > 1) per += (0.5 + 0.018 * bn) * (ce <= 4 ? 1.0 : 2.0);
-            const double cost = static_cast<double>(waves) * per;
-            if (cost < best_cost * 0.999) {
-                best_cost = cost;
-                best = GemmPlan{bn, ce, kb_per};
-            }
+        const PlanCost one = best_split(bi, bn, M, ntiles, KB, dev);
+        if (one.cost < best_cost * 0.999) {
+            best_cost = one.cost;
+            best = GemmPlan{bn, 1, {{0, ntiles, one.C, one.kb_per}, {0, 0, 1, KB}}};
+        }
+        // full waves of unsplit tiles, then the rest split
+        const int r1 = dev.gemm_clusters[bi][1];
+        const long units = static_cast<long>(ntiles) * mtiles;
+        if (r1 < 1 || units <= r1) continue;
+        const int t1 = static_cast<int>((units / r1) * r1 / mtiles);
+        if (t1 < 1 || t1 >= ntiles) continue;
+        const double full = static_cast<double>((static_cast<long>(t1) * mtiles + r1 - 1) / r1) *
+                            (4.0 + 0.38 * 4.0 * KB);
+        const PlanCost rest = best_split(bi, bn, M, ntiles - t1, KB, dev);
+        const double cost = full + rest.cost + 2.0;
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best = GemmPlan{bn, 2, {{0, t1, 1, KB}, {t1, ntiles, rest.C, rest.kb_per}}};
         }
     }
     return best;
@@ -540,9 +571,9 @@ cudaError_t gemm_setup(DeviceInfo& dev) {
 
 template <int BN>
 static cudaError_t launch_bn(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K,
-                             const GemmPlan& plan, cudaStream_t stream, unsigned int* err, int pdl) {
+                             const GemmLaunch& plan, cudaStream_t stream, unsigned int* err, int pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grp.tile_start[grp.count] * ((M + BN - 1) / BN), 1, plan.C);
+    cfg.gridDim = dim3((plan.t1 - plan.t0) * ((M + BN - 1) / BN), 1, plan.C);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = GemmCfg<BN>::kSmem;
     cfg.stream = stream;
@@ -563,17 +594,17 @@ static cudaError_t launch_bn(const WeightGroup& grp, const CUtensorMap& tmapX, i
     cfg.attrs = attr;
     cfg.numAttrs = na;
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, q4k_gemm_kernel<BN>, grp, tmapX, M, K, plan.C, plan.kb_per, pdl_flags,
-                              err);
+    return cudaLaunchKernelEx(&cfg, q4k_gemm_kernel<BN>, grp, tmapX, M, K, plan.t0, plan.C, plan.kb_per,
+                              pdl_flags, err);
 }
 
-cudaError_t launch_gemm(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K,
-                        const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev, int pdl) {
-    switch (plan.BN) {
-        case 32: return launch_bn<32>(grp, tmapX, M, K, plan, stream, dev.err, pdl);
-        case 64: return launch_bn<64>(grp, tmapX, M, K, plan, stream, dev.err, pdl);
-        case 128: return launch_bn<128>(grp, tmapX, M, K, plan, stream, dev.err, pdl);
-        case 256: return launch_bn<256>(grp, tmapX, M, K, plan, stream, dev.err, pdl);
+cudaError_t launch_gemm(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K, int BN,
+                        const GemmLaunch& part, cudaStream_t stream, const DeviceInfo& dev, int pdl) {
+    switch (BN) {
+        case 32: return launch_bn<32>(grp, tmapX, M, K, part, stream, dev.err, pdl);
+        case 64: return launch_bn<64>(grp, tmapX, M, K, part, stream, dev.err, pdl);
+        case 128: return launch_bn<128>(grp, tmapX, M, K, part, stream, dev.err, pdl);
+        case 256: return launch_bn<256>(grp, tmapX, M, K, part, stream, dev.err, pdl);
     }
     return cudaErrorInvalidValue;
 }

@@ -70,18 +70,23 @@ cudaError_t gemv_setup(DeviceInfo& dev);
 // tcgen05 GEMM for M >= 17 rows of bf16 activations over a group of weight
 // matrices (grp.maps as for the GEMV); tmapX: 3-D bf16 map {64, M, K / 64},
 // box {64, BN, gemm_x_steps(BN)}, 128-byte swizzle.
-struct GemmPlan {
-    int BN;      // tokens per tile (MMA N)
+struct GemmLaunch {
+    int t0, t1;  // global weight tiles [t0, t1) of the launch
     int C;       // K-split factor (cluster size along z)
     int kb_per;  // super-blocks per K-slice
+};
+struct GemmPlan {
+    int BN;             // tokens per tile (MMA N)
+    int nlaunch;        // 1, or 2: full waves of unsplit tiles, then the rest split in K
+    GemmLaunch part[2];
 };
 // ntiles: total 128-row weight tiles of the group.
 GemmPlan gemm_plan(int M, int ntiles, int K, const DeviceInfo& dev);
 // 64-k steps of X that one TMA copy of the GEMM brings for tile width BN: the
 // X tensor map is a 3-D view {64 k, M rows, K / 64} with box {64, BN, this}.
 int gemm_x_steps(int BN);
-cudaError_t launch_gemm(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K,
-                        const GemmPlan& plan, cudaStream_t stream, const DeviceInfo& dev, int pdl);
+cudaError_t launch_gemm(const WeightGroup& grp, const CUtensorMap& tmapX, int M, int K, int BN,
+                        const GemmLaunch& part, cudaStream_t stream, const DeviceInfo& dev, int pdl);
 // Sets the kernels' attributes and fills dev.gemm_clusters.
 cudaError_t gemm_setup(DeviceInfo& dev);
 
