@@ -16,9 +16,10 @@
 //               rows}, into their own ring, refilled as the dequantisers
 //               release a stage
 //   warp 19     TMA producer of the X tiles (k-major, 128-byte swizzle, into
-//               the k-step ring): one copy brings kXSteps consecutive 64-k
-//               tiles of BN token rows ({64 k, BN rows, kXSteps} of a 3-D view
-//               of X), refilled as the MMAs release the stages. (A TMA issue
+//               their own ring of k-steps): one copy brings kXSteps
+//               consecutive 64-k tiles of BN token rows ({64 k, BN rows,
+//               kXSteps} of a 3-D view of X), refilled as the MMAs of the
+//               copy it replaces complete. (A TMA issue
 //               costs its thread 150-350 cycles; one copy per 64-k step, from
 //               a thread that also fed the W ring, came only every ~800
 //               cycles, slower than the MMAs of a small-BN step.)
@@ -60,12 +61,12 @@ constexpr int kGemmThreads = 32 * (kGemmWarpX + 1);            // 640
 constexpr int kGemmWStageBytes = kGemmBM * kBlockBytes;   // 18432
 constexpr int kGemmAStageBytes = kGemmBM * 128;           // 16384
 
-// One ring of k-steps, each holding a dequantised A tile and a TMA-loaded X
-// (B) tile, as deep as shared memory allows: a step's full barrier completes
-// when its X bytes have landed and its dequantising group has arrived, and
-// one MMA commit releases both tiles, so an MMA-issuing warp waits once and
-// commits once per step. Each MMA warp has its own full barrier per stage
-// (k-step ks: warp ks % 2), visited every lcm(2, S) steps.
+// Two rings of k-steps: dequantised A tiles (S stages) and TMA-loaded X (B)
+// tiles (kXRing stages, kXSteps per copy). An MMA-issuing warp waits on the
+// A tile's full barrier (its dequantising group has arrived; one per (MMA
+// warp, stage): k-step ks is warp ks % 2's, visited every lcm(2, S) steps)
+// and the X copy's full barrier, and its commit releases the A stage; its
+// last commit in an X copy releases the copy's X stages.
 //
 // Release barriers: an mbarrier wait names only the parity of the phase it
 // waits for, so a waiter must never find its barrier two phases behind that
@@ -79,29 +80,32 @@ constexpr int kGemmAStageBytes = kGemmBM * 128;           // 16384
 // MMA warp each (L is even), so their phases follow the steps in order.
 template <int BN>
 struct GemmCfg {
-    static constexpr int kStages = BN == 256 ? 3 : 4;
+    static constexpr int kStages = BN == 256 ? 3 : 4;  // A ring (k-steps)
     // 64-k steps per X copy (the stages of one copy are consecutive in the ring)
     static constexpr int kXSteps = BN == 256 ? 1 : 4;
-    static_assert(kStages % kXSteps == 0, "X copies tile the ring");
-    static constexpr int kXSlots = kStages / kXSteps;  // X copies in flight
+    // X ring (k-steps), apart from the A ring: for narrow tiles two copies are
+    // in flight, so the next super-block's X lands while this one is consumed
+    static constexpr int kXRing = BN <= 64 ? 8 : kStages;
+    static_assert(kXRing % kXSteps == 0, "X copies tile the ring");
+    static constexpr int kXSlots = kXRing / kXSteps;  // X copies in flight
     // X-full barriers: with kXSteps > 1 (even) both MMA warps wait on every
     // copy, one barrier per slot; with one step per copy each warp waits only
-    // on its own steps' copies, so (as for the A tiles) one per (warp, stage)
-    static constexpr int kXBars = kXSteps == 1 ? 2 * kStages : kXSlots;
+    // on its own steps' copies, so (as for the A tiles) one per (warp, slot)
+    static constexpr int kXBars = kXSteps == 1 ? 2 * kXSlots : kXSlots;
+    static constexpr int kXL2 = kXSlots % 2 == 0 ? kXSlots : 2 * kXSlots;  // lcm(2, kXSlots)
     // packed-W ring (super-blocks), the rest of shared memory: a W box takes
-    // ~3.5 us from issue to landing under load (measured), so the ring, not
-    // the MMAs or the dequantisers, sets the pace of a narrow tile
-    static constexpr int kWStages = BN == 256 ? 4 : BN == 128 ? 5 : BN == 64 ? 7 : 8;
+    // several microseconds from issue to landing under load
+    static constexpr int kWStages = BN == 256 ? 4 : BN == 128 ? 5 : BN == 64 ? 5 : 7;
     static constexpr int kL = kStages % 4 == 0 ? kStages : kStages % 2 == 0 ? 2 * kStages : 4 * kStages;  // lcm(4, S)
     static constexpr int kL2 = kStages % 2 == 0 ? kStages : 2 * kStages;  // lcm(2, S)
     static constexpr int kBStageBytes = BN * 128;
     static constexpr int kOffA = 0;                                            // 1024-aligned
     static constexpr int kOffB = kOffA + kStages * kGemmAStageBytes;           // 1024-aligned
-    static constexpr int kOffW = kOffB + kStages * kBStageBytes;
+    static constexpr int kOffW = kOffB + kXRing * kBStageBytes;
     static constexpr int kOffBar = kOffW + kWStages * kGemmWStageBytes;
-    // barriers: w_full[W], w_empty[W], full[2][S] (A tiles), release[4][S],
-    // x_full[kXBars], acc_full
-    static constexpr int kNumBars = 2 * kWStages + 6 * kStages + kXBars + 1;
+    // barriers: w_full[W], w_empty[W], full[2][S] (A tiles), release[4][S] (A tiles),
+    // x_full[kXBars], x_release[kXSlots], acc_full
+    static constexpr int kNumBars = 2 * kWStages + 6 * kStages + kXBars + kXSlots + 1;
     static constexpr int kOffTmem = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffTmem + 16 + 1024;   // + alignment slack
     static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -189,14 +193,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t bfull = bw_empty + 8 * WS;
     const uint32_t brel = bfull + 8 * 2 * S;  // [4][S], see GemmCfg
     const uint32_t bxfull = brel + 8 * 4 * S;  // [kXBars], see GemmCfg
-    const uint32_t bacc = bxfull + 8 * Cfg::kXBars;
-    constexpr int XS = Cfg::kXSteps, XQ = Cfg::kXSlots;
+    const uint32_t bxrel = bxfull + 8 * Cfg::kXBars;  // [kXSlots]: the MMAs of copy j done
+    const uint32_t bacc = bxrel + 8 * Cfg::kXSlots;
+    constexpr int XS = Cfg::kXSteps, XQ = Cfg::kXSlots, SX = Cfg::kXRing;
     // the full barrier of X copy j and the parity of its phase
     auto xfull_bar = [&](int j) {
-        return bxfull + 8u * static_cast<uint32_t>(XS == 1 ? (j & 1) * S + j % S : j % XQ);
+        return bxfull + 8u * static_cast<uint32_t>(XS == 1 ? (j & 1) * XQ + (j >> 1) % XQ : j % XQ);
     };
-    auto xfull_parity = [](int j) { return static_cast<uint32_t>((XS == 1 ? j / Cfg::kL2 : j / XQ) & 1); };
-    // the release barrier of k-step ks, and the parity of its phase (ks >= S)
+    auto xfull_parity = [](int j) {
+        return static_cast<uint32_t>((XS == 1 ? (j >> 1) / XQ : j / XQ) & 1);
+    };
     auto rel_bar = [&](int ks) { return brel + 8u * static_cast<uint32_t>((ks & 3) * S + ks % S); };
     auto rel_parity = [](int ks) { return static_cast<uint32_t>(((ks - S) / Cfg::kL) & 1); };
     // the full barrier of k-step ks's A tile (MMA warp ks % 2) and the parity of its phase
@@ -211,6 +217,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int i = 0; i < 2 * S; ++i) mbar_init(bfull + 8 * i, kGemmBM);  // one dequantising group
         for (int i = 0; i < Cfg::kXBars; ++i) mbar_init(bxfull + 8 * i, 1);  // the X producer, with the bytes
+        // a copy's stages are free once every MMA warp with steps in it has
+        // committed its last one (both warps for 4-step copies)
+        for (int i = 0; i < XQ; ++i) mbar_init(bxrel + 8 * i, XS == 1 ? 1 : 2);
         for (int i = 0; i < 4 * S; ++i) mbar_init(brel + 8 * i, 1);  // one MMA commit
         mbar_init(bacc, 2);  // the last commit of each MMA warp
         fence_barrier_init();
@@ -257,23 +266,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == kGemmWarpX) {
         // ---------------------------------------------- X producer (TMA) ---
         // (after the preceding grid, like every warp but 0: X is its output).
-        // Copy j fills the stages of k-steps XS*j .. XS*j + XS - 1; they are
-        // free once the MMAs of the steps S earlier completed: the last even
-        // and the last odd of them (each MMA warp completes its steps in order).
+        // Copy j fills the X stages of k-steps XS*j .. XS*j + XS - 1; they are
+        // free once the MMAs of copy j - XQ have completed (its X-release
+        // barrier: the last commit of each MMA warp with steps in that copy).
         if (lane == 0) {
             tma_prefetch_desc(&tmapX);
             const uint64_t pol_x = policy_evict_last();
             const int nx = nks / XS;
             int j = 0;
             for (; j < nx; ++j) {
-                const int klast = XS * j + XS - 1;
-                bool ok = true;
-                for (int k = klast - (XS > 1 ? 1 : 0); k <= klast && ok; ++k)
-                    ok = k < S || mbar_wait(rel_bar(k), rel_parity(k), err);
-                if (!ok) break;
+                if (j >= XQ && !mbar_wait(bxrel + 8 * (j % XQ), ((j / XQ) - 1) & 1, err)) break;
                 const uint32_t xb = xfull_bar(j);
                 mbar_arrive_expect_tx(xb, XS * Cfg::kBStageBytes);
-                tma_load_3d_hint(sbase + Cfg::kOffB + ((XS * j) % S) * Cfg::kBStageBytes, &tmapX, 0, m0,
+                tma_load_3d_hint(sbase + Cfg::kOffB + ((XS * j) % SX) * Cfg::kBStageBytes, &tmapX, 0, m0,
                                  ks0 + XS * j, xb, pol_x);
             }
             // as for W: at most the last XQ copies issued can be landing
@@ -298,11 +303,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             if (elect_one()) {
                 const uint64_t a0 = sw128_desc(sbase + Cfg::kOffA + s * kGemmAStageBytes);
-                const uint64_t b0 = sw128_desc(sbase + Cfg::kOffB + s * Cfg::kBStageBytes);
+                const uint64_t b0 = sw128_desc(sbase + Cfg::kOffB + (ks % SX) * Cfg::kBStageBytes);
 #pragma unroll
                 for (int kk = 0; kk < kGemmKStep / 16; ++kk)  // +32 bytes per k16 = +2 in the address field
                     tc_mma_bf16(dacc, a0 + 2 * kk, b0 + 2 * kk, idesc, (ks >= 2) || kk != 0);
-                tc_commit(rel_bar(ks + S));  // releases the stage for k-step ks + S
+                tc_commit(rel_bar(ks + S));  // releases the A stage for k-step ks + S
+                // this warp's last step of its X copy releases the copy's X stages
+                if (XS == 1 || (ks % XS) >= XS - 2) tc_commit(bxrel + 8 * ((ks / XS) % XQ));
             }
             __syncwarp();
         }
