@@ -80,7 +80,11 @@ constexpr int kGemmAStageBytes = kGemmBM * 128;           // 16384
 // MMA warp each (L is even), so their phases follow the steps in order.
 template <int BN>
 struct GemmCfg {
-    static constexpr int kStages = BN == 256 ? 3 : 4;  // A ring (k-steps)
+    // A ring (k-steps): a dequantising group writes every fourth step, so a
+    // ring of 4 gives each group one stage and chains its writes to the MMAs
+    // of its previous step; 6 lets it run ahead (32-token tiles: 83 -> 80 us
+    // per Qwen3-8B-shaped layer)
+    static constexpr int kStages = BN == 256 ? 3 : BN == 32 ? 6 : 4;
     // 64-k steps per X copy (the stages of one copy are consecutive in the ring)
     static constexpr int kXSteps = BN == 256 ? 1 : 4;
     // X ring (k-steps), apart from the A ring: for narrow tiles two copies are
@@ -95,7 +99,7 @@ struct GemmCfg {
     static constexpr int kXL2 = kXSlots % 2 == 0 ? kXSlots : 2 * kXSlots;  // lcm(2, kXSlots)
     // packed-W ring (super-blocks), the rest of shared memory: a W box takes
     // several microseconds from issue to landing under load
-    static constexpr int kWStages = BN == 256 ? 4 : BN == 128 ? 5 : BN == 64 ? 5 : 7;
+    static constexpr int kWStages = BN == 256 ? 4 : 5;
     static constexpr int kL = kStages % 4 == 0 ? kStages : kStages % 2 == 0 ? 2 * kStages : 4 * kStages;  // lcm(4, S)
     static constexpr int kL2 = kStages % 2 == 0 ? kStages : 2 * kStages;  // lcm(2, S)
     static constexpr int kBStageBytes = BN * 128;
