@@ -88,8 +88,11 @@ struct GemmCfg {
     // 64-k steps per X copy (the stages of one copy are consecutive in the ring)
     static constexpr int kXSteps = BN == 256 ? 1 : 4;
     // X ring (k-steps), apart from the A ring: for narrow tiles two copies are
-    // in flight, so the next super-block's X lands while this one is consumed
-    static constexpr int kXRing = BN <= 64 ? 8 : kStages;
+    // in flight, so the next super-block's X lands while this one is consumed;
+    // at BN = 256 the 32 KB copy of each k-step paces the MMAs, and a fourth X
+    // stage (with 2 W stages to make room) measured 169 -> 163 us per
+    // Qwen3-8B-shaped layer of 512 rows
+    static constexpr int kXRing = BN <= 64 ? 8 : BN == 256 ? 4 : kStages;
     static_assert(kXRing % kXSteps == 0, "X copies tile the ring");
     static constexpr int kXSlots = kXRing / kXSteps;  // X copies in flight
     // X-full barriers: with kXSteps > 1 (even) both MMA warps wait on every
@@ -99,7 +102,7 @@ struct GemmCfg {
     static constexpr int kXL2 = kXSlots % 2 == 0 ? kXSlots : 2 * kXSlots;  // lcm(2, kXSlots)
     // packed-W ring (super-blocks), the rest of shared memory: a W box takes
     // several microseconds from issue to landing under load
-    static constexpr int kWStages = BN == 256 ? 4 : 5;
+    static constexpr int kWStages = BN == 256 ? 2 : 5;
     static constexpr int kL = kStages % 4 == 0 ? kStages : kStages % 2 == 0 ? 2 * kStages : 4 * kStages;  // lcm(4, S)
     static constexpr int kL2 = kStages % 2 == 0 ? kStages : 2 * kStages;  // lcm(2, S)
     static constexpr int kBStageBytes = BN * 128;
