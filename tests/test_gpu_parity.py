@@ -182,6 +182,30 @@ def test_gemm_ragged(q4k, oracle_mod, M):
         _check_matmul(q4k, oracle_mod, Wh, Wh.to(DEV), N, K, X, TOL_GEMM)
 
 
+@pytest.mark.parametrize("M", [40, 64, 100, 128, 200])
+def test_gemm_tile_widths(q4k, oracle_mod, M):
+    """Every tile width's ring configuration: 64-token tiles (X ring of two 4-step
+    copies), 128-token tiles (X ring as deep as the A ring), 256-token tiles (one
+    X step per copy, 4 X stages), over several weight tiles and a K of 8 super-blocks."""
+    N, K = 300, 2048
+    Wh = synth.weight_rows(6500 + M, N, K)
+    X = synth.activations(6600 + M, M, K, torch.bfloat16)
+    _check_matmul(q4k, oracle_mod, Wh, Wh.to(DEV), N, K, X, TOL_GEMM)
+
+
+@pytest.mark.parametrize("M", [32, 512])
+def test_gemm_partial_wave_as_two_launches(q4k, oracle_mod, M):
+    """A matrix whose unsplit CTAs end in a partial wave: the plan runs the full
+    waves' tiles unsplit and the rest of the tiles as a second, K-split launch.
+    Sampled output rows cover both launches' tiles (and the boundary)."""
+    N, K = 200 * 128, 1024
+    Wd = synth.weight_rows(6700 + M, N, K, device=DEV)
+    rows = sorted(set(_sample_rows(N, n=192, seed=M)) | {151 * 128 + 127, 152 * 128, N - 1})
+    W_rows = synth.weight_sample_rows(6700 + M, N, K, rows)
+    X = synth.activations(6800 + M, M, K, torch.bfloat16)
+    _check_matmul(q4k, oracle_mod, None, Wd, N, K, X, TOL_GEMM, rows=rows, W_rows=W_rows)
+
+
 def test_gemm_long_k(q4k, oracle_mod):
     N, K, M = 256, 12288, 300
     Wh = synth.weight_rows(6000, N, K)
