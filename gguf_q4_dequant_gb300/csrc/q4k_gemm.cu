@@ -19,16 +19,16 @@
 //               their own ring of k-steps): one copy brings kXSteps
 //               consecutive 64-k tiles of BN token rows ({64 k, BN rows,
 //               kXSteps} of a 3-D view of X), refilled as the MMAs of the
-//               copy it replaces complete. (A TMA issue
-//               costs its thread 150-350 cycles; one copy per 64-k step, from
-//               a thread that also fed the W ring, came only every ~800
-//               cycles, slower than the MMAs of a small-BN step.)
+//               copy it replaces complete. (A TMA issue costs its thread
+//               150-350 cycles; one copy per 64-k step, from a thread that
+//               also fed the W ring, came only every ~800 cycles, slower than
+//               the MMAs of a small-BN step.)
 //   warps 1, 18 MMA issuers: warp 1 takes the even k-steps, warp 18 the odd
 //               ones, each into its own TMEM accumulator (the epilogue adds
 //               the two), so the barrier waits and issue latencies of two
 //               steps overlap (the warp runs the loop, one elected lane
-//               issues: 4 MMAs of K = 16 and one commit per step); warp 1
-//               also allocates TMEM
+//               issues 4 MMAs of K = 16 and a commit per step, plus one at
+//               its last step of an X copy); warp 1 also allocates TMEM
 //   warps 2..17 dequantisers, four groups of 128 threads: thread t <-> weight
 //               row t % 128 of the 64-k chunk c = t / 128 of every super-block
 //               (k-step 4 sb + c). A thread reads its row's header and the
