@@ -32,7 +32,12 @@
 //   neighbouring qs words form one 64-bit register pair, so a 64-bit mask
 //   yields the same nibble of both words as an fp32 pair for the paired FMA
 //   (fma.rn.f32x2); the top three nibbles of each word are first brought down
-//   by one 64-bit shift by 12. Each activation is pre-scaled once per
+//   by one 64-bit shift by 12. The one-row kernel of launches that do not split
+//   K instead moves bits 20..31 of each word down (the subnormal u*2^-149 of
+//   the 12-bit field u) and splits u into its three codes with products by
+//   2^-8 and 2^-4 rounded toward zero -- floor on the subnormal grid -- and
+//   exact FMAs: work moved from the integer pipe (logic and shifts issue at
+//   half the FMA rate) to the FMA pipe. Each activation is pre-scaled once per
 //   (super-block, row of X) by 2^(E+149-4p) by the activation warp and stored
 //   in the order the pairs consume them, so a mask and half a paired FMA per
 //   weight give q*x*2^E with a single rounding and no int->float conversion.
@@ -131,8 +136,12 @@ __device__ __forceinline__ int block_exponent(float amax) {
 //   [A A C C E E G G | B B D D F F H H]   (each letter: word u, word u+1)
 // where A,C,E,G are the low nibbles of bytes 0..3 and B,D,F,H the high ones,
 // so this lane's 8 values go to the 8 floats at c*64 + v*16 + 8h, slot 2j+up.
-// The nibble positions p (value q*2^(4p-149)) are A0 C2 E4 G3 and B1 D3 F2 H4.
+// The consumer reads the codes as q*2^(4p-149): p is the nibble's position in
+// its word for the five codes in bits 0..19 (A0 B1 C2 D3 E4); F, G and H are
+// brought down by 12 bits first (F2 G3 H4), or, with SPLIT, split out of bits
+// 20..31 on the FMA pipe (F0 G0 H0).
 // Also stores the sub-block sums scaled by 2^E and 2^-E (as two factors).
+template <bool SPLIT>
 __device__ __forceinline__ void scale_activations(const float (&v)[8], int lane, float* xs,
                                                   float* xsum, float* inv) {
     const int h = (lane >> 2) & 1;
@@ -153,7 +162,8 @@ __device__ __forceinline__ void scale_activations(const float (&v)[8], int lane,
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         // nibble position of byte j's low (h = 0) or high (h = 1) nibble
-        const int p = h ? ((0x4231 >> (4 * j)) & 0xF) : ((0x3420 >> (4 * j)) & 0xF);
+        const int p = SPLIT ? (h ? ((0x0031 >> (4 * j)) & 0xF) : ((0x0420 >> (4 * j)) & 0xF))
+                            : (h ? ((0x4231 >> (4 * j)) & 0xF) : ((0x3420 >> (4 * j)) & 0xF));
         const int t = base - 4 * p;
         const float fa = exp2i(t >> 1), fb = exp2i(t - (t >> 1));
         o[2 * j] = (v[j] * fa) * fb;          // up = 0: word u
@@ -179,9 +189,32 @@ template <int MT>
 struct XPrefetch {
     static constexpr int kRows = MT <= 4 ? MT : 0;
 };
+// fp32 pairs (both halves equal) for splitting a 12-bit field of codes:
+// 2^-8, 2^-4 and -256, -16.
+constexpr uint64_t kPairP2m8 = 0x3B8000003B800000ull;
+constexpr uint64_t kPairP2m4 = 0x3D8000003D800000ull;
+constexpr uint64_t kPairM256 = 0xC3800000C3800000ull;
+constexpr uint64_t kPairM16 = 0xC1800000C1800000ull;
+
+// a * b elementwise on fp32 pairs, rounded toward zero (subnormals kept).
+__device__ __forceinline__ uint64_t mul2_rz(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Bits 20..31 of each 32-bit half of p, moved down (zero-filled).
+__device__ __forceinline__ uint64_t top12_pair(uint64_t p) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r)
+        : "r"(static_cast<uint32_t>(p) >> 20), "r"(static_cast<uint32_t>(p >> 32) >> 20));
+    return r;
+}
+
 // One consumer lane: the contribution of one super-block of its row, scaled by
-// 2^E (acc[m] for each activation row m).
-template <int MT>
+// 2^E (acc[m] for each activation row m). SPLIT selects how the codes in bits
+// 20..31 of each word are unpacked (scale_activations<SPLIT> matches it).
+template <int MT, bool SPLIT>
 __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, const float* xsum,
                                           float (&acc)[MT]) {
     const uint4 h = *reinterpret_cast<const uint4*>(P);
@@ -220,15 +253,32 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const uint64_t Pw = wp[v];
-            const uint64_t Sw = Pw >> 12;  // bytes 2 (high nibble) and 3 of each word, brought down
+            // the five codes in bits 0..19 of each word, masked in place: the
+            // fp32 bit pattern is the subnormal q*2^(4p-149)
             const uint64_t qA = Pw & 0x0000000F0000000Full;  // byte 0 low   p0
             const uint64_t qB = Pw & 0x000000F0000000F0ull;  // byte 0 high  p1
             const uint64_t qC = Pw & 0x00000F0000000F00ull;  // byte 1 low   p2
             const uint64_t qD = Pw & 0x0000F0000000F000ull;  // byte 1 high  p3
             const uint64_t qE = Pw & 0x000F0000000F0000ull;  // byte 2 low   p4
-            const uint64_t qF = Sw & 0x00000F0000000F00ull;  // byte 2 high  p2
-            const uint64_t qG = Sw & 0x0000F0000000F000ull;  // byte 3 low   p3
-            const uint64_t qH = Sw & 0x000F0000000F0000ull;  // byte 3 high  p4
+            uint64_t qF, qG, qH;
+            if constexpr (SPLIT) {
+                // bits 20..31 of each word moved down, u = F + 16*G + 256*H:
+                // the subnormal u*2^-149. A product with 2^-8 rounded toward zero
+                // lands on floor(u/256)*2^-149 (the subnormal grid is 2^-149) and
+                // the FMA that takes it back off is exact, so two such steps give
+                // F, G and H as q*2^-149: four FMA-pipe operations where the
+                // masks below take five integer ones
+                const uint64_t T = top12_pair(Pw);
+                qH = mul2_rz(T, kPairP2m8);               // byte 3 high
+                const uint64_t t = fma2(qH, kPairM256, T);  // F + 16*G
+                qG = mul2_rz(t, kPairP2m4);               // byte 3 low
+                qF = fma2(qG, kPairM16, t);               // byte 2 high
+            } else {
+                const uint64_t Sw = Pw >> 12;  // bits 20..31 of each word brought down to 8..19
+                qF = Sw & 0x00000F0000000F00ull;  // byte 2 high  p2
+                qG = Sw & 0x0000F0000000F000ull;  // byte 3 low   p3
+                qH = Sw & 0x000F0000000F0000ull;  // byte 3 high  p4
+            }
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const ulonglong2* xp = reinterpret_cast<const ulonglong2*>(xs + m * 256 + 64 * c + 16 * v);
@@ -266,7 +316,7 @@ __device__ __forceinline__ void block_dot(const uint8_t* P, const float* xs, con
 // shares tiles and splits K into C slices of kb_per super-blocks. With C > 1
 // every cluster owns exactly one tile. amax == nullptr: Y_i is written; else
 // (one matrix) no Y is written and each row's argmax key goes to amax[m].
-template <int MT, bool XB>
+template <int MT, bool XB, bool SPLIT>
 __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks)
     q4k_gemv_kernel(const __grid_constant__ WeightGroup grp, const void* __restrict__ X, int M, int K,
                 int C, int kb_per, int pdl_flags, unsigned long long* amax, unsigned int* err) {
@@ -377,7 +427,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 if (!mbar_wait(bar_empty + 8 * s, ((st / S) & 1) ^ 1, err)) break;
 #pragma unroll
                 for (int m = 0; m < PF; ++m)
-                    scale_activations(cur[m], lane, xs + m * 256, xsum + m * 8, inv + 2 * m);
+                    scale_activations<SPLIT>(cur[m], lane, xs + m * 256, xsum + m * 8, inv + 2 * m);
             } else {
                 // rows in batches of 8 whose loads are all in flight together
                 // (the first batch before the wait for the slot)
@@ -395,7 +445,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                     }
 #pragma unroll
                     for (int j = 0; j < B; ++j)
-                        scale_activations(v[j], lane, xs + (m0 + j) * 256, xsum + (m0 + j) * 8, inv + 2 * (m0 + j));
+                        scale_activations<SPLIT>(v[j], lane, xs + (m0 + j) * 256, xsum + (m0 + j) * 8, inv + 2 * (m0 + j));
                 }
             }
             __syncwarp();
@@ -455,7 +505,7 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
                 const uint8_t* P = smem + Cfg::kOffW + s * kGemvStageBytes + r * kBlockBytes;
                 const float* xs = xs_ring + (s * MT + m0) * 256;
                 const float* xsm = xsum_ring + (s * MT + m0) * 8;
-                block_dot<ML>(P, xs, xsm, acc);
+                block_dot<ML, SPLIT>(P, xs, xsm, acc);
                 const float* inv = inv_ring + (s * MT + m0) * 2;
 #pragma unroll
                 for (int m = 0; m < ML; ++m) y[m] += (acc[m] * inv[2 * m]) * inv[2 * m + 1];
@@ -520,16 +570,27 @@ __global__ void __launch_bounds__(GemvCfg<MT>::kThreads, GemvCfg<MT>::kMinBlocks
 
 template <int MT, bool XB>
 static cudaError_t set_attr(DeviceInfo& dev, int slot) {
-    cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, XB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<MT>::kSmem);
+    const auto kern = q4k_gemv_kernel<MT, XB, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<MT>::kSmem);
     if (e != cudaSuccess) return e;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, q4k_gemv_kernel<MT, XB>, GemvCfg<MT>::kThreads,
-                                                      GemvCfg<MT>::kSmem);
-    dev.gemv_occ[XB ? 1 : 0][slot] = occ < 1 ? 1 : occ;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, GemvCfg<MT>::kThreads, GemvCfg<MT>::kSmem);
     if (e != cudaSuccess) return e;
+    if constexpr (MT == 1) {
+        // the variant that unpacks part of the codes on the FMA pipe, for
+        // launches that do not split K (it runs without clusters); the CTA
+        // slots of the plan are the fewer of the two kernels'
+        const auto ks = q4k_gemv_kernel<MT, XB, true>;
+        e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<MT>::kSmem);
+        if (e != cudaSuccess) return e;
+        int occ_s = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_s, ks, GemvCfg<MT>::kThreads, GemvCfg<MT>::kSmem);
+        if (e != cudaSuccess) return e;
+        occ = occ_s < occ ? occ_s : occ;
+    }
+    dev.gemv_occ[XB ? 1 : 0][slot] = occ < 1 ? 1 : occ;
     if (GemvCfg<MT>::kMaxSplit > 8 &&
-        cudaFuncSetAttribute(q4k_gemv_kernel<MT, XB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess)
         (void)cudaGetLastError();  // then the occupancy query below reports 0 for C > 8
     for (int c = 2; c <= GemvCfg<MT>::kMaxSplit; ++c) {
@@ -545,7 +606,7 @@ static cudaError_t set_attr(DeviceInfo& dev, int slot) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, q4k_gemv_kernel<MT, XB>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
             (void)cudaGetLastError();
             n = 0;
         }
@@ -625,7 +686,17 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
     // pdl_flags bit 0: the producer also waits for the preceding grid before
     // streaming W (cleared only when the caller allows weight prefetch).
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, XB>, grp, X, M, K, C, kb_per, pdl_flags, amax,
+    // M = 1 without a K split (long, persistent launches, bound by the issue
+    // rate of the SMs that hold two CTAs): the variant that moves part of the
+    // unpacking to the FMA pipe. Split launches, whose few stages per CTA are
+    // latency-bound after the release, keep the shorter dependency chains.
+    // Measured (M = 1): 34816 x 5120 gate/up 23.1 -> 21.9 us; 7168 x 5120
+    // q/k/v (split 4 ways) 6.9 -> 7.2 us with the variant.
+    auto kern = q4k_gemv_kernel<MT, XB, false>;
+    if constexpr (MT == 1) {
+        if (C == 1) kern = q4k_gemv_kernel<MT, XB, true>;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, grp, X, M, K, C, kb_per, pdl_flags, amax,
                               dev.err);
 }
 

@@ -159,6 +159,32 @@ def test_gemv_activation_scales(q4k, oracle_mod):
     _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, torch.zeros(2, K), TOL_GEMV)
 
 
+@pytest.mark.parametrize("N,K", [(96, 2048), (300, 256), (40960, 1024)])
+def test_gemv_activation_scales_one_and_two_rows(q4k, oracle_mod, N, K):
+    """The CUDA-core decode kernel (M <= 2) on the same extreme activation rows.
+    96 x 2048 splits K across a cluster; with one super-block per row (K = 256)
+    or at least as many tiles as CTA slots (40960 rows) the launch does not
+    split K, and the one-row kernel then unpacks the codes of bits 20..31 of
+    each qs word on the FMA pipe (activations pre-scaled for that layout)."""
+    Wh = synth.weight_rows(11 + N, N, K)
+    Wd = Wh.to(DEV)
+    base = synth.activations(12, 6, K)
+    scale = torch.ones(6, K)
+    scale[0, :256] = 1e30
+    scale[0, 256:512] = 1e-30
+    scale[1, :] = 1e-38
+    scale[2, 512:768] = 0.0
+    scale[3, ::7] = 3e4
+    scale[4, :] = 0.0
+    X = (base * scale).float()
+    for r in range(6):
+        _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X[r:r + 1].contiguous(), TOL_GEMV)
+    for r in range(0, 6, 2):
+        _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, X[r:r + 2].contiguous(), TOL_GEMV)
+        Xb = X[r:r + 2].clamp(-3e38, 3e38).to(torch.bfloat16)
+        _check_matmul(q4k, oracle_mod, Wh, Wd, N, K, Xb[:1].contiguous(), TOL_GEMV)
+
+
 def test_fp32_large_m_runs_in_16_row_slices(q4k, oracle_mod):
     N, K = 200, 1024
     Wh = synth.weight_rows(9, N, K)
