@@ -32,8 +32,8 @@
 //   neighbouring qs words form one 64-bit register pair, so a 64-bit mask
 //   yields the same nibble of both words as an fp32 pair for the paired FMA
 //   (fma.rn.f32x2); the top three nibbles of each word are first brought down
-//   by one 64-bit shift by 12. The one-row kernel of launches that do not split
-//   K instead moves bits 20..31 of each word down (the subnormal u*2^-149 of
+//   by one 64-bit shift by 12. The one-row fp32 kernel of launches that do not
+//   split K instead moves bits 20..31 of each word down (the subnormal u*2^-149 of
 //   the 12-bit field u) and splits u into its three codes with products by
 //   2^-8 and 2^-4 rounded toward zero -- floor on the subnormal grid -- and
 //   exact FMAs: work moved from the integer pipe (logic and shifts issue at
@@ -576,7 +576,7 @@ static cudaError_t set_attr(DeviceInfo& dev, int slot) {
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, GemvCfg<MT>::kThreads, GemvCfg<MT>::kSmem);
     if (e != cudaSuccess) return e;
-    if constexpr (MT == 1) {
+    if constexpr (MT == 1 && !XB) {
         // the variant that unpacks part of the codes on the FMA pipe, for
         // launches that do not split K (it runs without clusters); the CTA
         // slots of the plan are the fewer of the two kernels'
@@ -686,14 +686,15 @@ static cudaError_t launch_mt(const WeightGroup& grp, const void* X, int M, int K
     // pdl_flags bit 0: the producer also waits for the preceding grid before
     // streaming W (cleared only when the caller allows weight prefetch).
     const int pdl_flags = (pdl == 2) ? 0 : 1;
-    // M = 1 without a K split (long, persistent launches, bound by the issue
-    // rate of the SMs that hold two CTAs): the variant that moves part of the
-    // unpacking to the FMA pipe. Split launches, whose few stages per CTA are
-    // latency-bound after the release, keep the shorter dependency chains.
-    // Measured (M = 1): 34816 x 5120 gate/up 23.1 -> 21.9 us; 7168 x 5120
-    // q/k/v (split 4 ways) 6.9 -> 7.2 us with the variant.
+    // M = 1, fp32 X, without a K split (long, persistent launches, bound by
+    // the issue rate of the SMs that hold two CTAs): the variant that moves
+    // part of the unpacking to the FMA pipe. Split launches, whose few stages
+    // per CTA are latency-bound after the release, keep the shorter dependency
+    // chains. Measured (M = 1): 34816 x 5120 gate/up 23.1 -> 21.9 us; 7168 x
+    // 5120 q/k/v (split 4 ways) 6.9 -> 7.2 us with the variant; with bf16 X
+    // the Qwen3-14B-shaped sweep 1.93 -> 1.98 ms, so bf16 X keeps the masks.
     auto kern = q4k_gemv_kernel<MT, XB, false>;
-    if constexpr (MT == 1) {
+    if constexpr (MT == 1 && !XB) {
         if (C == 1) kern = q4k_gemv_kernel<MT, XB, true>;
     }
     return cudaLaunchKernelEx(&cfg, kern, grp, X, M, K, C, kb_per, pdl_flags, amax,

@@ -164,8 +164,8 @@ def test_gemv_activation_scales_one_and_two_rows(q4k, oracle_mod, N, K):
     """The CUDA-core decode kernel (M <= 2) on the same extreme activation rows.
     96 x 2048 splits K across a cluster; with one super-block per row (K = 256)
     or at least as many tiles as CTA slots (40960 rows) the launch does not
-    split K, and the one-row kernel then unpacks the codes of bits 20..31 of
-    each qs word on the FMA pipe (activations pre-scaled for that layout)."""
+    split K, and the one-row fp32 kernel then unpacks the codes of bits 20..31
+    of each qs word on the FMA pipe (activations pre-scaled for that layout)."""
     Wh = synth.weight_rows(11 + N, N, K)
     Wd = Wh.to(DEV)
     base = synth.activations(12, 6, K)
