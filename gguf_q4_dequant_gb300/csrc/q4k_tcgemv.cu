@@ -112,7 +112,7 @@ struct TcCfg {
     // wfull[WS] wempty[WS] afull[AS] aempty[AS] bfull[BS] bempty[BS] hfull[HR] hempty[HR]
     // accfull[4] accempty[4] red fin
     static constexpr int kNumBars = 2 * kWS + 2 * kAS + 2 * kBS + 2 * kHR + 8 + 2;
-    static constexpr int kOffTmem = kOffBar + kNumBars * 8;
+    static constexpr int kOffTmem = kOffBar + kNumBars * 8;  // TMEM address; +8: a word holding 0
     static constexpr int kSmem = kOffTmem + 16 + 1024;  // + alignment slack
     static_assert(kSmem <= 232448, "shared memory");
 };
@@ -165,9 +165,11 @@ __global__ void __launch_bounds__(TcCfg<MT, XB>::kThreads, 1)
     const uint32_t b_red = b_accempty + 32;
     const uint32_t b_fin = b_red + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmem);
+    uint32_t* zero_slot = tmem_slot + 2;
     float* red = reinterpret_cast<float*>(smem + Cfg::kOffRed);
 
     if (threadIdx.x == 0) {
+        *zero_slot = 0u;
         for (int i = 0; i < WS; ++i) {
             mbar_init(b_wfull + 8 * i, 1);                 // producer, with the stage's bytes
             mbar_init(b_wempty + 8 * i, kTcExpThreads);    // every expansion thread
@@ -273,6 +275,9 @@ __global__ void __launch_bounds__(TcCfg<MT, XB>::kThreads, 1)
         const int t = threadIdx.x - 32 * Cfg::kWarpExp;
         const int c = t >> 6;              // warp-uniform (two warps per chunk)
         const int r0 = t & 63;
+        // 0, read from shared memory so that the compiler cannot fold the
+        // data dependence built from it below
+        const uint32_t zero = *reinterpret_cast<volatile uint32_t*>(zero_slot);
         for (int sb = 0; sb < total; ++sb) {
             const int ws = sb % WS;
             if (!mbar_wait(b_wfull + 8 * ws, (sb / WS) & 1, err)) break;
@@ -284,8 +289,11 @@ __global__ void __launch_bounds__(TcCfg<MT, XB>::kThreads, 1)
                 q[rr][1] = *reinterpret_cast<const uint4*>(P + 32 + 32 * c);
                 hd[rr] = c == 0 ? *reinterpret_cast<const uint4*>(P) : make_uint4(0u, 0u, 0u, 0u);
             }
-            fence_proxy_async_smem();  // generic reads of the stage before its next TMA write
-            mbar_arrive(b_wempty + 8 * ws);
+            // the stage goes back to the producer only after these reads have
+            // returned (its next TMA write must not overtake them): the
+            // release's barrier address depends on the loaded values
+            const uint32_t dep = (q[0][0].x ^ q[0][1].x ^ q[1][0].x ^ q[1][1].x ^ hd[0].x ^ hd[1].x) & zero;
+            mbar_arrive(b_wempty + 8 * ws + dep);
             if (c == 0) {  // the rows' headers, for the readout
                 const int hs = sb % HR;
                 if (!mbar_wait(b_hempty + 8 * hs, ((sb / HR) & 1) ^ 1, err)) break;
